@@ -1,0 +1,199 @@
+"""Seeded synthetic inputs for MLA attention over a paged FP8-e4m3 latent KV cache.
+
+This module only draws inputs: it holds none of the attention arithmetic, and both
+the CUDA path and the float64 oracle consume exactly what it returns.
+
+Shapes follow the pages on MLA serving: every cached position is one row of 576
+FP8 bytes (read here as a 512-wide latent followed by a 64-wide RoPE part), the
+cache is paged, and query heads per rank are 8, 12 or 16
+("Scaling Kimi K3 on AMD Instinct MI355X", sections "缓存可复用，还要能一致地恢复"
+and "并行度必须适配真正的形状"; "MI355X Kimi K2.5 vLLM AITER 7x speedup",
+section "PR #35850 修复了什么").
+
+Recipe (fixed draw order, one CPU ``torch.Generator`` seeded per workload):
+  1. sequence lengths (``seq_lens`` include the ``n_q`` new positions),
+  2. a random permutation of physical pool pages (identity for a contiguous cache),
+  3. queries ``q ~ N(0, 1)`` rounded to bfloat16, layout ``[B][n_q][H][576]``,
+  4. latent rows ``x ~ N(0, 1)`` in float32, one per logical cache slot (whole pages,
+     so slots past ``seq_lens[b]`` in a sequence's last page hold valid codes too),
+     quantised with one per-tensor scale ``kv_scale = amax / 448`` as
+     ``e4m3_rne(clamp(x / kv_scale, -448, 448))``. The clamp comes first because
+     ``x / kv_scale`` can round a hair above 448 and the float8 cast does not
+     saturate.
+``sm_scale`` is ``1 / sqrt(192)`` for every workload.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import torch
+
+D = 576  # bytes (= e4m3 codes) per cached position
+DV = 512  # latent width; V is the first DV codes of a row
+PAGE = 64  # positions per page
+SM_SCALE = 1.0 / math.sqrt(192.0)
+
+
+@dataclasses.dataclass
+class MlaInputs:
+    """One seeded workload, all tensors on the CPU.
+
+    pool        uint8  [num_pages, page_size, 576]  e4m3 codes
+    page_table  int32  [B, max_pages]               physical page per logical page, -1 unused
+    seq_lens    int32  [B]                          cached positions per sequence (incl. n_q new)
+    q           bfloat16 [B, n_q, H, 576]
+    kv_scale    float  dequantised value = e4m3(code) * kv_scale
+    sm_scale    float
+    """
+
+    name: str
+    pool: torch.Tensor
+    page_table: torch.Tensor
+    seq_lens: torch.Tensor
+    q: torch.Tensor
+    kv_scale: float
+    sm_scale: float
+    page_size: int
+
+    @property
+    def B(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def n_q(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def H(self) -> int:
+        return int(self.q.shape[2])
+
+    def kv_bytes_touched(self) -> int:
+        """Bytes of cache rows the attention must read once: sum of seq_lens * 576."""
+        return int(self.seq_lens.to(torch.int64).sum().item()) * D
+
+
+def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """float32 -> e4m3fn codes (uint8) with round-to-nearest-even after clamping."""
+    y = (x / scale).clamp_(-448.0, 448.0)
+    return y.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _latent_codes(n_rows: int, g: torch.Generator, chunk: int = 1 << 16):
+    """Draw n_rows x 576 N(0,1) values and quantise them with scale = amax / 448.
+
+    Two passes over the same generator state keep peak host memory small: the
+    first finds amax, the second replays the identical draws and quantises them.
+    """
+    state = g.get_state()
+    amax = 0.0
+    done = 0
+    while done < n_rows:
+        n = min(chunk, n_rows - done)
+        x = torch.randn(n, D, generator=g, dtype=torch.float32)
+        amax = max(amax, float(x.abs().max().item()))
+        done += n
+    g.set_state(state)
+    scale = amax / 448.0
+    codes = torch.empty(n_rows, D, dtype=torch.uint8)
+    done = 0
+    while done < n_rows:
+        n = min(chunk, n_rows - done)
+        x = torch.randn(n, D, generator=g, dtype=torch.float32)
+        codes[done:done + n] = quantize_e4m3(x, scale)
+        done += n
+    return codes, float(scale)
+
+
+def make_inputs(
+    name: str,
+    seq_lens: Sequence[int] | None = None,
+    *,
+    H: int,
+    n_q: int = 1,
+    B: Optional[int] = None,
+    len_range: Optional[tuple[int, int]] = None,
+    page_size: int = PAGE,
+    contiguous: bool = False,
+    seed: int = 0,
+    sm_scale: float = SM_SCALE,
+) -> MlaInputs:
+    """Build one workload. Either ``seq_lens`` or (``B``, ``len_range``) is given;
+    ``len_range`` draws lengths uniformly from the closed interval."""
+    g = torch.Generator().manual_seed(seed)
+    # 1. lengths
+    if seq_lens is None:
+        assert B is not None and len_range is not None
+        lo, hi = len_range
+        lens = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64)
+    else:
+        lens = torch.tensor(list(seq_lens), dtype=torch.int64)
+    B = int(lens.numel())
+    pages_per_seq = [(int(L) + page_size - 1) // page_size for L in lens.tolist()]
+    total_pages = sum(pages_per_seq)
+    max_pages = max(1, max(pages_per_seq) if pages_per_seq else 1)
+    # 2. physical page permutation
+    if contiguous:
+        perm = torch.arange(total_pages, dtype=torch.int64)
+    else:
+        perm = torch.randperm(total_pages, generator=g)
+    page_table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    logical = 0
+    for b, np_ in enumerate(pages_per_seq):
+        page_table[b, :np_] = perm[logical:logical + np_].to(torch.int32)
+        logical += np_
+    # 3. queries
+    q = torch.randn(B, n_q, H, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    # 4. latent rows in logical order, then scattered into the pool
+    codes, kv_scale = _latent_codes(total_pages * page_size, g)
+    codes = codes.view(total_pages, page_size, D)
+    pool = torch.empty_like(codes)
+    pool[perm] = codes
+    return MlaInputs(
+        name=name,
+        pool=pool,
+        page_table=page_table,
+        seq_lens=lens.to(torch.int32),
+        q=q,
+        kv_scale=kv_scale,
+        sm_scale=float(sm_scale),
+        page_size=page_size,
+    )
+
+
+# --- the five named workloads ---------------------------------------------------
+
+def tiny_decode(seed: int = 0) -> MlaInputs:
+    """Batch 1, 12 heads, 1 query, 1024 cached positions, contiguous cache."""
+    return make_inputs("tiny_decode_b1_h12_l1024", [1024], H=12, n_q=1, contiguous=True, seed=seed)
+
+
+def batched_paged_decode(seed: int = 0) -> MlaInputs:
+    """Batch 32, 12 heads, 1 query, lengths uniform in [4096, 16384], random pages."""
+    return make_inputs("batched_paged_decode_b32_h12_l4k-16k", None, H=12, n_q=1, B=32,
+                       len_range=(4096, 16384), seed=seed)
+
+
+def long_history_decode(H: int = 12, seed: int = 0) -> MlaInputs:
+    """Batch 1, one query, 142,000 cached positions, H in {8, 12, 16}."""
+    return make_inputs(f"long_history_decode_b1_h{H}_l142000", [142000], H=H, n_q=1, seed=seed)
+
+
+def spec_verify(seed: int = 0) -> MlaInputs:
+    """Batch 8, 12 heads, 4 verify positions on a 32,768 prefix (32,772 cached)."""
+    return make_inputs("spec_verify_b8_h12_q4_l32772", [32768 + 4] * 8, H=12, n_q=4, seed=seed)
+
+
+def causal_prefill(T: int = 8192, prefix: int = 32768, H: int = 12, seed: int = 0) -> MlaInputs:
+    """One sequence: a T-token chunk on a `prefix`-token cached history, causal."""
+    return make_inputs(f"causal_prefill_t{T}_p{prefix}_h{H}", [prefix + T], H=H, n_q=T, seed=seed)
+
+
+WORKLOADS = {
+    "tiny_decode": tiny_decode,
+    "batched_paged_decode": batched_paged_decode,
+    "long_history_decode": long_history_decode,
+    "spec_verify": spec_verify,
+    "causal_prefill": causal_prefill,
+}

@@ -1,0 +1,260 @@
+"""Pins that tie the float64 oracle to something other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with:
+  * a library routine (torch's float8_e4m3fn and bfloat16 conversions; float64
+    ``scaled_dot_product_attention`` and ``logsumexp`` on CPU),
+  * a closed form (constant V, a single visible key, q = 0, duplicated keys),
+  * an invariant the pages state (heads attend independently, so padding or
+    permuting heads changes nothing for the real ones; partial attention over key
+    ranges merged by normalisation statistics equals attention over the whole range;
+    a new position sees its prefix and itself only).
+The pins are plain functions so that ``test_oracle_mutants.py`` can run all of them
+against deliberately broken builds of the oracle and check each break is caught.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from mla_latent_kv_attention_gb300 import workloads as W
+
+D, DV = 576, 512
+
+
+def _tiny(seed=1, lens=(7, 11), H=3, n_q=2, page_size=4, contiguous=False):
+    return W.make_inputs("tiny", list(lens), H=H, n_q=n_q, page_size=page_size,
+                         contiguous=contiguous, seed=seed)
+
+
+def _gather_keys(inp, b):
+    """Codes of the cached rows of sequence b in logical order, via the page table."""
+    L = int(inp.seq_lens[b])
+    ps = inp.page_size
+    idx = [int(inp.page_table[b, n // ps]) for n in range(L)]
+    return torch.stack([inp.pool[idx[n], n % ps] for n in range(L)]) if L else torch.empty(0, D,
+                                                                                           dtype=torch.uint8)
+
+
+def sdpa_reference(inp):
+    """Library reference: decode codes with torch's float8_e4m3fn, then float64 SDPA with
+    K = whole row (broadcast over heads), V = first 512 entries, explicit causal mask."""
+    B, n_q, H = inp.B, inp.n_q, inp.H
+    out = torch.zeros(B, n_q, H, DV, dtype=torch.float64)
+    lse = torch.zeros(B, n_q, H, dtype=torch.float64)
+    for b in range(B):
+        L = int(inp.seq_lens[b])
+        k = _gather_keys(inp, b).view(torch.float8_e4m3fn).to(torch.float64) * inp.kv_scale
+        v = k[:, :DV]
+        q = inp.q[b].to(torch.float64).permute(1, 0, 2)  # [H, n_q, 576]
+        mask = torch.zeros(n_q, L, dtype=torch.bool)
+        for j in range(n_q):
+            mask[j, :max(0, L - n_q + j + 1)] = True
+        o = F.scaled_dot_product_attention(q, k.expand(H, L, D), v.expand(H, L, DV),
+                                           attn_mask=mask, scale=inp.sm_scale)
+        s = (q @ k.T) * inp.sm_scale
+        s = s.masked_fill(~mask, float("-inf"))
+        out[b] = o.permute(1, 0, 2)
+        lse[b] = torch.logsumexp(s, dim=-1).permute(1, 0)
+    return out.numpy(), lse.numpy()
+
+
+def pin_e4m3_all_codes(orc):
+    """All 256 codes against torch's float8_e4m3fn, plus the OCP E4M3 anchor values:
+    max normal 448 (S.1111.110), min normal 2^-6, max subnormal 0.875*2^-6, min
+    subnormal 2^-9, NaN only at S.1111.111."""
+    lib_vals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    for c in range(256):
+        mine = orc.e4m3_value(c)
+        ref = float(lib_vals[c])
+        if math.isnan(ref):
+            assert math.isnan(mine), c
+        else:
+            assert mine == ref, (c, mine, ref)
+    assert orc.e4m3_value(0x7E) == 448.0 and orc.e4m3_value(0xFE) == -448.0
+    assert orc.e4m3_value(0x08) == 2.0 ** -6
+    assert orc.e4m3_value(0x07) == 0.875 * 2.0 ** -6
+    assert orc.e4m3_value(0x01) == 2.0 ** -9
+    assert math.isnan(orc.e4m3_value(0x7F)) and math.isnan(orc.e4m3_value(0xFF))
+
+
+def pin_bf16(orc):
+    """bfloat16 bit patterns against torch's bfloat16 -> float64 conversion."""
+    g = torch.Generator().manual_seed(3)
+    bits = torch.randint(0, 1 << 16, (4096,), generator=g, dtype=torch.int32)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # skip inf/nan exponents
+    vals = bits.to(torch.int16).view(torch.bfloat16).to(torch.float64)
+    for bt, v in zip(bits.tolist(), vals.tolist()):
+        assert orc.bf16_value(bt & 0xFFFF) == v, (bt, v)
+
+
+def pin_brute_force_sdpa(orc):
+    """Tiny paged workloads (pages of 4 positions, ragged lengths, several new positions)
+    against float64 SDPA; also a contiguous single-sequence decode."""
+    for kw in (dict(seed=1), dict(seed=2, lens=(5,), H=2, n_q=1, contiguous=True),
+               dict(seed=4, lens=(9, 3, 12), H=3, n_q=3)):
+        inp = _tiny(**kw)
+        out, lse = orc.attention(inp)
+        ref_out, ref_lse = sdpa_reference(inp)
+        np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def pin_constant_v(orc):
+    """Every row's first 512 codes equal -> output equals that V whatever the scores."""
+    inp = _tiny(seed=5, lens=(9,), H=2, n_q=1)
+    row = inp.pool[0, 0, :DV].clone()
+    inp.pool[:, :, :DV] = row
+    out, _ = orc.attention(inp)
+    v = row.view(torch.float8_e4m3fn).to(torch.float64).numpy() * inp.kv_scale
+    for h in range(inp.H):
+        np.testing.assert_allclose(out[0, 0, h], v, rtol=1e-13, atol=0)
+
+
+def pin_single_key(orc):
+    """One visible key -> output is that row's V and lse is its score."""
+    inp = _tiny(seed=6, lens=(1,), H=3, n_q=1)
+    out, lse = orc.attention(inp)
+    codes = inp.pool[int(inp.page_table[0, 0]), 0]
+    k = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy() * inp.kv_scale
+    for h in range(inp.H):
+        q = inp.q[0, 0, h].to(torch.float64).numpy()
+        np.testing.assert_allclose(out[0, 0, h], k[:DV], rtol=1e-13, atol=0)
+        assert abs(lse[0, 0, h] - inp.sm_scale * float(q @ k)) <= 1e-12 * max(1, abs(lse[0, 0, h]))
+
+
+def pin_zero_query(orc):
+    """q = 0 -> uniform weights: output = mean of the visible V rows, lse = ln(#visible)."""
+    inp = _tiny(seed=7, lens=(10,), H=2, n_q=3)
+    inp.q.zero_()
+    out, lse = orc.attention(inp)
+    k = _gather_keys(inp, 0).view(torch.float8_e4m3fn).to(torch.float64).numpy() * inp.kv_scale
+    for j in range(3):
+        vis = 10 - 3 + j + 1
+        for h in range(2):
+            np.testing.assert_allclose(out[0, j, h], k[:vis, :DV].mean(axis=0), rtol=1e-12,
+                                       atol=1e-15)
+            assert abs(lse[0, j, h] - math.log(vis)) < 1e-12
+
+
+def pin_duplicate_key(orc):
+    """Two identical keys instead of one -> lse grows by exactly ln 2, output unchanged."""
+    one = W.make_inputs("one", [1], H=2, n_q=1, page_size=4, seed=8)
+    two = W.make_inputs("two", [2], H=2, n_q=1, page_size=4, seed=8)
+    two.pool[int(two.page_table[0, 0]), 1] = two.pool[int(two.page_table[0, 0]), 0]
+    one.pool[int(one.page_table[0, 0]), 0] = two.pool[int(two.page_table[0, 0]), 0]
+    one.q.copy_(two.q)
+    one.kv_scale = two.kv_scale
+    o1, l1 = orc.attention(one)
+    o2, l2 = orc.attention(two)
+    np.testing.assert_allclose(l2 - l1, math.log(2.0), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o2, o1, rtol=1e-13, atol=0)
+
+
+def pin_split_merge(orc):
+    """Attention over [0, c) and [c, L) merged by their lse equals attention over [0, L),
+    for every split point c (including empty ranges)."""
+    inp = _tiny(seed=9, lens=(13,), H=2, n_q=1)
+    full_out, full_lse = orc.attention(inp)
+    for h in range(2):
+        for c in range(0, 14):
+            o1, l1 = orc.attention_range(inp, 0, 0, h, 0, c)
+            o2, l2 = orc.attention_range(inp, 0, 0, h, c, 13)
+            mo, ml = orc.merge_lse(np.stack([o1, o2])[:, None, :], np.array([[l1], [l2]]))
+            np.testing.assert_allclose(mo[0], full_out[0, 0, h], rtol=1e-12, atol=1e-15)
+            assert abs(ml[0] - full_lse[0, 0, h]) < 1e-12
+    # a three-way split with one empty middle piece
+    o = [orc.attention_range(inp, 0, 0, 1, a, b) for a, b in ((0, 5), (5, 5), (5, 13))]
+    mo, ml = orc.merge_lse(np.stack([x[0] for x in o])[:, None, :],
+                           np.array([[x[1]] for x in o]))
+    np.testing.assert_allclose(mo[0], full_out[0, 0, 1], rtol=1e-12, atol=1e-15)
+
+
+def pin_merge_weights(orc):
+    """Merge against its closed form on random partials: weights exp(lse_s - lse) sum to 1
+    and lse equals log(sum exp(lse_s)) computed by torch.logsumexp."""
+    rng = np.random.default_rng(10)
+    po = rng.standard_normal((5, 7, DV))
+    pl = rng.standard_normal((5, 7)) * 4
+    pl[2, 3] = -np.inf
+    out, lse = orc.merge_lse(po, pl)
+    ref_lse = torch.logsumexp(torch.from_numpy(pl), dim=0).numpy()
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-13)
+    w = np.exp(pl - ref_lse[None, :])
+    np.testing.assert_allclose((w[:, :, None] * po).sum(0), out, rtol=1e-12, atol=1e-14)
+    # all-empty row
+    out2, lse2 = orc.merge_lse(po[:2, :1], np.full((2, 1), -np.inf))
+    assert lse2[0] == -np.inf and np.all(out2 == 0)
+
+
+def pin_permuted_pages(orc):
+    """Moving pages around the pool (and the table with them) changes nothing."""
+    inp = _tiny(seed=11, lens=(11, 6), H=2, n_q=2)
+    out, lse = orc.attention(inp)
+    g = torch.Generator().manual_seed(12)
+    perm = torch.randperm(inp.pool.shape[0], generator=g)
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel())
+    pool2 = torch.empty_like(inp.pool)
+    pool2[perm] = inp.pool
+    pt2 = inp.page_table.clone()
+    m = pt2 >= 0
+    pt2[m] = perm[pt2[m].long()].to(torch.int32)
+    inp.pool, inp.page_table = pool2, pt2
+    out2, lse2 = orc.attention(inp)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def pin_head_padding_and_permutation(orc):
+    """12 heads padded to 16 with zero heads or repeated heads leave the 12 real heads
+    exactly unchanged; permuting heads permutes outputs exactly."""
+    inp = _tiny(seed=13, lens=(9,), H=12, n_q=1)
+    out, lse = orc.attention(inp)
+    for pad in ("zero", "repeat"):
+        q16 = torch.zeros(1, 1, 16, D, dtype=torch.bfloat16)
+        q16[:, :, :12] = inp.q
+        if pad == "repeat":
+            q16[:, :, 12:] = inp.q[:, :, :4]
+        inp16 = W.MlaInputs("pad", inp.pool, inp.page_table, inp.seq_lens, q16, inp.kv_scale,
+                            inp.sm_scale, inp.page_size)
+        o16, l16 = orc.attention(inp16)
+        assert np.array_equal(o16[:, :, :12], out) and np.array_equal(l16[:, :, :12], lse)
+    perm = torch.randperm(12, generator=torch.Generator().manual_seed(14))
+    inpp = W.MlaInputs("perm", inp.pool, inp.page_table, inp.seq_lens, inp.q[:, :, perm],
+                       inp.kv_scale, inp.sm_scale, inp.page_size)
+    op, lp = orc.attention(inpp)
+    assert np.array_equal(op, out[:, :, perm.numpy()]) and np.array_equal(lp, lse[:, :, perm.numpy()])
+
+
+def pin_causal_prefix(orc):
+    """New position j of a chunk equals a one-query decode whose cache ends at that
+    position: prefill row i == decode with L = prefix + i + 1."""
+    prefix, T = 5, 4
+    inp = _tiny(seed=15, lens=(prefix + T,), H=2, n_q=T)
+    out, lse = orc.attention(inp)
+    for i in range(T):
+        dec = W.MlaInputs("dec", inp.pool, inp.page_table,
+                          torch.tensor([prefix + i + 1], dtype=torch.int32),
+                          inp.q[:, i:i + 1].clone(), inp.kv_scale, inp.sm_scale, inp.page_size)
+        o, l = orc.attention(dec)
+        np.testing.assert_allclose(o[0, 0], out[0, i], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(l[0, 0], lse[0, i], rtol=1e-13)
+
+
+def pin_sampled_rows(orc):
+    """The row-list entry point returns exactly the rows of the full computation."""
+    inp = _tiny(seed=16, lens=(9, 12), H=3, n_q=3)
+    out, lse = orc.attention(inp)
+    rows = np.array([[1, 2, 0], [0, 0, 2], [1, 0, 1], [0, 2, 2]])
+    o, l = orc.attention_rows(inp, rows)
+    for i, (b, j, h) in enumerate(rows):
+        assert np.array_equal(o[i], out[b, j, h]) and l[i] == lse[b, j, h]
+
+
+ALL_PINS = [
+    pin_e4m3_all_codes, pin_bf16, pin_brute_force_sdpa, pin_constant_v, pin_single_key,
+    pin_zero_query, pin_duplicate_key, pin_split_merge, pin_merge_weights, pin_permuted_pages,
+    pin_head_padding_and_permutation, pin_causal_prefix, pin_sampled_rows,
+]
