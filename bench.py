@@ -1,0 +1,346 @@
+"""Benchmark: MLA decode over a paged FP8 latent cache on GB300.
+
+One step = one pass of the whole decode hot path (split planning, paged FP8 fetch,
+scores, online softmax, value accumulation, split-KV LSE merge) over one batch of the
+batched paged decode workload: 32 sequences, 12 heads, 1 query each, lengths uniform
+in [4096, 16384], 64-position pages randomly placed in one pool, seed 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. `value` is achieved algorithmic HBM GB/s (cache rows read once +
+queries + outputs + lse + lengths + page-table entries, divided by the device time of a
+step), summed over ranks. Inputs sit in HBM; several full copies are rotated so that no
+step finds its inputs in the 129 MB L2. Multi-GPU runs are independent replicas (the
+decode path has no exchange step on one node): weak scaling, no collective in the data
+path. `--impl reference` times the float64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/layer & HBM GB/s vs peak; prefill tok/s & tensor-pipe %"
+WORKLOAD = "batched_paged_decode"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, parts[1:]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return None
+        inside = [r for t, r in rows if self.t0 - 0.05 <= t <= self.t1 + 0.05]
+        window = "timed region"
+        if not inside:  # timed region shorter than the sampling interval: nearest samples
+            inside = [min(rows, key=lambda tr: abs(tr[0] - 0.5 * (self.t0 + self.t1)))[1]]
+            window = "nearest sample to a timed region shorter than the 20 ms sampling period"
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def kernel_traffic(kernel_file):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if the
+    summary was taken on the current source of that kernel; else None."""
+    summary = os.path.join(ROOT, "profiles", "decode_split_kernel_batched_paged_decode.md")
+    src = os.path.join(ROOT, "mla_latent_kv_attention_gb300", "csrc", kernel_file)
+    if not (os.path.exists(summary) and os.path.exists(src)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    text = open(summary).read()
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if m_src and m_tr and m_src.group(1) == digest:
+        return float(m_tr.group(1))
+    return None
+
+
+def bench_reference(args, world, rank):
+    """The float64 CPU oracle on the same workload (each step one full oracle pass)."""
+    if rank != 0:
+        return
+    import oracle
+    from mla_latent_kv_attention_gb300 import accounting, workloads as W
+    oracle.build()
+    inp = W.batched_paged_decode()
+    nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), 1, inp.H)
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.attention(inp, n_threads=cores)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.attention(inp, n_threads=cores)
+        times.append(time.perf_counter() - t)
+    ms = 1e3 * sum(times) / len(times)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "B": inp.B, "H": inp.H, "n_q": 1,
+                                         "seq_lens": "uniform[4096,16384] seed 0", "page_size": 64},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "the whole workload (all 32 sequences x 12 heads) per step"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def bench_ours(args, world, rank, local):
+    import torch
+
+    import mla_latent_kv_attention_gb300 as mla
+    from mla_latent_kv_attention_gb300 import accounting, workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, _, peak_src = load_peaks()
+    inp = W.batched_paged_decode()
+    H, B = inp.H, inp.B
+    nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), 1, H)
+    kv_bytes = inp.pool.numel()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(2, math.ceil(3 * l2 / kv_bytes))
+    sets = []
+    for _ in range(copies):
+        kv = mla.KVCache.from_inputs(inp, dev)
+        q = inp.q[:, 0].contiguous().to(dev)
+        out = torch.empty(B, H, 512, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, H, dtype=torch.float32, device=dev)
+        ws = mla.workspace(mla.MLA_OP_DECODE, B, H, 1, dev)
+        sets.append((kv, q, out, lse, ws))
+
+    def step(i, ev=None):
+        kv, q, out, lse, ws = sets[i % copies]
+        mla.mla_decode(kv, q, inp.sm_scale, out=out, lse=lse, ws=ws)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    launches_per_step = mla.mla_last_launch_count()
+    status = mla.mla_read_status(sets[0][4])
+    if status != 0:
+        raise RuntimeError(f"device status {mla.STATUS.get(status)}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kst = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ksp = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stream = torch.cuda.current_stream()
+    for e in kst + ksp:  # create the underlying events before handing them to the library
+        e.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 or True else None
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    for i in range(args.steps):
+        mla.mla_set_profile_events(kst[i], ksp[i])
+        starts[i].record(stream)
+        step(i)
+        stops[i].record(stream)
+    mla.mla_set_profile_events(None, None)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
+    kern_ms = [s.elapsed_time(e) for s, e in zip(kst, ksp)]
+    ms = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms, world, dev)
+    kms = sum(kern_ms) / len(kern_ms)
+    value = world * nbytes / (ms / 1e3) / 1e9
+
+    # End to end through the public API with host buffers: pinned host inputs copied in,
+    # the decode, the outputs read back, every step.
+    h_pool = inp.pool.pin_memory()
+    h_pt = inp.page_table.pin_memory()
+    h_sl = inp.seq_lens.pin_memory()
+    h_q = inp.q[:, 0].contiguous().pin_memory()
+    h_out = torch.empty(B, H, 512, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(B, H, dtype=torch.float32).pin_memory()
+    kv, q, out, lse, ws = sets[0]
+    h2d = h_pool.numel() + h_pt.numel() * 4 + h_sl.numel() * 4 + h_q.numel() * 2
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def e2e_step():
+        kv.pool.copy_(h_pool, non_blocking=True)
+        kv.page_table.copy_(h_pt, non_blocking=True)
+        kv.seq_lens.copy_(h_sl, non_blocking=True)
+        q.copy_(h_q, non_blocking=True)
+        mla.mla_decode(kv, q, inp.sm_scale, out=out, lse=lse, ws=ws)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    barrier(world)
+
+    line = None
+    if rank == 0:
+        achieved = nbytes / (kms / 1e3) / 1e9
+        traffic = kernel_traffic("mla_attn_v0.cu")
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "us_per_layer": ms * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32-acc (e4m3 cache, bf16 q/out)",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "H": H, "n_q": 1,
+                       "seq_lens": "uniform[4096,16384] seed 0",
+                       "total_cached_positions": int(inp.seq_lens.sum()), "page_size": 64,
+                       "algorithmic_bytes_per_step": nbytes,
+                       "l2": f"inputs rotated over {copies} resident copies (>= 3x L2)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic,
+                         "kernel": "split-KV attention kernel (CUDA events around its launch)",
+                         "kernel_ms": kms, "peak_source": f"{peak_src} hbm_gbs"},
+            "e2e": {"value": world * nbytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+    return line
+
+
+def cpu_baseline(line):
+    import oracle
+    from mla_latent_kv_attention_gb300 import accounting, workloads as W
+    oracle.build()
+    inp = W.batched_paged_decode()
+    nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), 1, inp.H)
+    cores = os.cpu_count() or 1
+    t = time.perf_counter()
+    oracle.attention(inp, n_threads=cores)
+    dt = time.perf_counter() - t
+    line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores,
+                            "kind": "oracle", "seconds": dt,
+                            "sample": "the whole workload once (32 sequences x 12 heads, float64)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        bench_reference(args, world, rank)
+        return
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    barrier(world)
+    line = bench_ours(args, world, rank, local)
+    if rank == 0:
+        if world == 1:
+            cpu_baseline(line)
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

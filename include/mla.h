@@ -1,0 +1,170 @@
+/*
+ * mla.h -- C ABI of libmla: Multi-head Latent Attention (MLA) over a paged FP8-e4m3
+ * latent KV cache, for one GB300 (sm_103a) GPU.
+ *
+ * The operation (all entry points): every cached position is one row of 576 e4m3 codes,
+ * read as a 512-wide latent followed by a 64-wide RoPE part. Keys are whole rows, values
+ * their first 512 entries, both dequantised as e4m3(code) * kv_scale ("MI355X Kimi K2.5
+ * vLLM AITER 7x speedup", section "PR #35850 修复了什么": keys and values share one latent
+ * space, FP8 KV cache; "Scaling Kimi K3 on AMD Instinct MI355X", section
+ * "缓存可复用，还要能一致地恢复": 576 FP8 bytes per position). For query row
+ * (sequence b, new position j, head h) with bfloat16 query q[576]:
+ *     s_n   = sm_scale * sum_d q[d] * k_n[d]                 for visible keys n
+ *     lse   = ln sum_n exp(s_n)                              (natural log, float32)
+ *     out   = sum_n exp(s_n - lse) * v_n                     (bfloat16, round to nearest even)
+ * Key n is visible to new position j iff n <= seq_lens[b] - n_q + j: the n_q new positions
+ * are already written to the cache and are causal among themselves. Heads attend
+ * independently ("Scaling Kimi K3 ...", section "并行度必须适配真正的形状"), so any
+ * head count 1..16 runs as is; nothing is padded in memory.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" point to GPU global memory the caller owns; the library
+ *    never allocates, frees or synchronises on the compute entry points. All work is
+ *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default stream)
+ *    and is stream-ordered with the caller's other work.
+ *  - bfloat16 tensors are passed as their 16-bit patterns (uint16_t / void*).
+ *  - Argument errors the host can see return an error status immediately and enqueue
+ *    nothing. Errors only the GPU can see (a page index outside the pool, a length larger
+ *    than the page table holds, a bounded wait that gave up) are written to a status word
+ *    inside the workspace and read back with mla_read_status(). No entry point aborts,
+ *    asserts or traps.
+ *  - Layouts are dense, row-major, with the innermost dimension last as written.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_D 576       /* e4m3 codes per cached position (512 latent + 64 RoPE) */
+#define MLA_DV 512      /* value width: the first 512 codes of a row              */
+#define MLA_MAX_HEADS 16
+#define MLA_MAX_NQ 4    /* verify positions per sequence                          */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned pointer          */
+  MLA_ERR_UNSUPPORTED = 2, /* heads outside 1..16, n_q outside 1..4, page size not 64k */
+  MLA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than mla_workspace_size()   */
+  MLA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute query)      */
+  MLA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel gave up           */
+  MLA_ERR_BOUNDS = 6       /* device: page index outside the pool or length > table    */
+} mla_status_t;
+
+typedef enum { MLA_OP_DECODE = 0, MLA_OP_VERIFY = 1, MLA_OP_PREFILL = 2 } mla_op_t;
+
+/*
+ * The paged latent cache.
+ *   pool              device, [num_pages][page_size][576] e4m3 codes; 16-byte aligned.
+ *   num_pages         pages in the pool (page indices must lie in [0, num_pages)).
+ *   page_size         positions per page; 64 or a multiple of 64.
+ *   page_table        device, [B][page_table_stride] int32: physical page of logical page p
+ *                     of sequence b. Entries past a sequence's last page are never read.
+ *   page_table_stride entries per row of page_table (>= pages of the longest sequence).
+ *   seq_lens          device, [B] int32: cached positions of each sequence, including the
+ *                     n_q new ones. 0 is allowed (the rows come out as out = 0,
+ *                     lse = -inf). Negative or larger than page_table_stride * page_size:
+ *                     MLA_ERR_BOUNDS in the status word, that sequence treated as empty.
+ *   kv_scale          dequantised value = e4m3(code) * kv_scale, for K and V alike.
+ * A contiguous cache is the identity page table.
+ */
+typedef struct mla_kv {
+  const uint8_t* pool;
+  int64_t num_pages;
+  int32_t page_size;
+  const int32_t* page_table;
+  int64_t page_table_stride;
+  const int32_t* seq_lens;
+  float kv_scale;
+} mla_kv_t;
+
+/*
+ * Bytes of workspace the given call needs on `device` (a CUDA ordinal). The workspace
+ * holds the split plan, the per-split partial outputs and the status word; it must be
+ * 256-byte aligned and stay untouched until the call's work has finished on its stream.
+ * For MLA_OP_PREFILL pass B = 1 and n_q = T. Returns 0 for unsupported arguments.
+ */
+size_t mla_workspace_size(mla_op_t op, int B, int H, int n_q, int device);
+
+/*
+ * Decode: one new position per sequence (n_q = 1).
+ *   q    device, [B][H][576] bfloat16, 16-byte aligned
+ *   out  device, [B][H][512] bfloat16
+ *   lse  device, [B][H] float32 (natural log); may be NULL if not wanted
+ * The key axis of long sequences is split across the GPU's SMs; per-split results are
+ * combined with the log-sum-exp merge ("Scaling Kimi K3 ...", section
+ * "缓存可复用，还要能一致地恢复": partial attention merged by normalisation statistics).
+ */
+mla_status_t mla_decode(const mla_kv_t* kv, const void* q, int B, int H, float sm_scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
+ * Speculative verify: n_q in 1..4 new positions per sequence, causal among themselves
+ * ("Scaling Kimi K3 ...", section "并行度必须适配真正的形状": four verify positions per
+ * sequence). n_q = 1 is exactly mla_decode.
+ *   q    device, [B][n_q][H][576] bfloat16
+ *   out  device, [B][n_q][H][512] bfloat16
+ *   lse  device, [B][n_q][H] float32, or NULL
+ */
+mla_status_t mla_verify(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
+                        float sm_scale, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
+ * Causal chunked prefill of one sequence: T new positions attend to the cached prefix
+ * and causally to each other ("AMD MI355X推理Kimi K3：吞吐量超NVIDIA，首字优化显著",
+ * section "首Token等待优化：简单补零解决大问题": long cold prefill through the MLA
+ * prefill kernel). kv describes one sequence (seq_lens[0] = prefix + T).
+ *   q    device, [T][H][576] bfloat16
+ *   out  device, [T][H][512] bfloat16
+ *   lse  device, [T][H] float32, or NULL
+ */
+mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float sm_scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * Log-sum-exp merge of S partial results per row ("Scaling Kimi K3 ...", section
+ * "缓存可复用，还要能一致地恢复"): lse = ln sum_s exp(lse_s),
+ * out = sum_s exp(lse_s - lse) * out_s. Partials with lse_s = -inf carry weight 0; a row
+ * whose partials are all -inf gets out = 0, lse = -inf.
+ *   part_out  device, [S][R][512] float32 (each partial already normalised)
+ *   part_lse  device, [S][R] float32 (natural log)
+ *   out       device, [R][512] bfloat16
+ *   lse       device, [R] float32, or NULL
+ * This is the step a position-sharded (DCP) deployment runs after gathering partials.
+ */
+mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, int64_t R,
+                           void* out, float* lse, void* stream);
+
+/*
+ * Synchronises `stream`, then returns the status word the last call on this workspace
+ * left (MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT), or MLA_ERR_CUDA if the stream itself
+ * reports an error. Each compute call resets the word when its work starts.
+ */
+mla_status_t mla_read_status(const void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* mla_status_string(mla_status_t status);
+
+/* Number of kernel launches the last compute call on this host thread enqueued. */
+int mla_last_launch_count(void);
+
+/*
+ * Profiling hook. When both are non-NULL, the next compute calls on this host thread
+ * record `start` (a cudaEvent_t passed as void*) on their stream just before the main
+ * attention kernel and `stop` just after it, so cudaEventElapsedTime() gives that
+ * kernel's own duration. Pass NULL, NULL to switch it off. The events stay owned by the
+ * caller.
+ */
+void mla_set_profile_events(void* start, void* stop);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H */

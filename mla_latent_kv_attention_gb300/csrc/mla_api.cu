@@ -1,0 +1,208 @@
+// mla_api.cu -- the C ABI of libmla: argument checks, workspace layout, launches.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_internal.cuh"
+
+namespace {
+
+thread_local int g_last_launches = 0;
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+void prof_mark(cudaEvent_t e, cudaStream_t s) {
+  if (g_prof_start && g_prof_stop) cudaEventRecord(e, s);
+}
+
+int sm_count(int device) {
+  static int cache[64] = {0};
+  if (device >= 0 && device < 64 && cache[device] > 0) return cache[device];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (device >= 0 && device < 64) cache[device] = n;
+  return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+mla_status_t check_kv(const mla_kv_t* kv) {
+  if (!kv || !kv->pool || !kv->page_table || !kv->seq_lens) return MLA_ERR_INVALID_ARG;
+  if (kv->num_pages < 0 || kv->page_table_stride < 1) return MLA_ERR_INVALID_ARG;
+  if (kv->page_size <= 0 || kv->page_size % 64 != 0) return MLA_ERR_UNSUPPORTED;
+  if (!aligned(kv->pool, 16) || !aligned(kv->page_table, 4) || !aligned(kv->seq_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+mla::AttnParams base_params(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
+                            float sm_scale, void* out, float* lse) {
+  mla::AttnParams p = {};
+  p.pool = kv->pool;
+  p.num_pages = kv->num_pages;
+  p.page_size = kv->page_size;
+  p.page_table = kv->page_table;
+  p.pt_stride = kv->page_table_stride;
+  p.seq_lens = kv->seq_lens;
+  p.kv_scale = kv->kv_scale;
+  p.sm_scale = sm_scale;
+  p.q = static_cast<const uint16_t*>(q);
+  p.B = B;
+  p.n_q = n_q;
+  p.H = H;
+  p.R = n_q * H;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  return p;
+}
+
+mla_status_t current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H, float sm_scale,
+                       void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  g_last_launches = 0;
+  mla_status_t st = check_kv(kv);
+  if (st != MLA_OK) return st;
+  if (B < 0) return MLA_ERR_INVALID_ARG;
+  if (H < 1 || H > MLA_MAX_HEADS || n_q < 1 || n_q > MLA_MAX_NQ) return MLA_ERR_UNSUPPORTED;
+  if (!q || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return MLA_ERR_WORKSPACE;
+  int dev;
+  if ((st = current_device(&dev)) != MLA_OK) return st;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const mla::WsLayout w = mla::ws_layout(B, n_q * H, sms);
+  if (ws_bytes < w.total) return MLA_ERR_WORKSPACE;
+  if (B == 0) return MLA_OK;
+  mla::AttnParams p = base_params(kv, q, B, n_q, H, sm_scale, out, lse);
+  char* base = static_cast<char*>(ws);
+  p.hdr = reinterpret_cast<mla::WsHeader*>(base + w.hdr);
+  p.units = reinterpret_cast<mla::Unit*>(base + w.units);
+  p.seqs = reinterpret_cast<mla::SeqUnits*>(base + w.seqs);
+  p.part_lse = reinterpret_cast<float*>(base + w.part_lse);
+  p.part_out = reinterpret_cast<float*>(base + w.part_out);
+  p.max_units = w.max_units;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mla::launch_plan(p, mla::kUnitsPerSm * sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+  ++g_last_launches;
+  prof_mark(g_prof_start, s);
+  if (mla::launch_attn_v0(p, false, 0, s) != cudaSuccess) return MLA_ERR_CUDA;
+  prof_mark(g_prof_stop, s);
+  ++g_last_launches;
+  if (mla::launch_merge(p, s) != cudaSuccess) return MLA_ERR_CUDA;
+  ++g_last_launches;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_workspace_size(mla_op_t op, int B, int H, int n_q, int device) {
+  if (H < 1 || H > MLA_MAX_HEADS || B < 0) return 0;
+  if (op == MLA_OP_PREFILL) {
+    if (B != 1 || n_q < 0) return 0;
+    return sizeof(mla::WsHeader);
+  }
+  if (op == MLA_OP_DECODE) n_q = 1;
+  if (n_q < 1 || n_q > MLA_MAX_NQ) return 0;
+  const int sms = sm_count(device);
+  if (sms <= 0) return 0;
+  return mla::ws_layout(B, n_q * H, sms).total;
+}
+
+mla_status_t mla_decode(const mla_kv_t* kv, const void* q, int B, int H, float sm_scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  return run_split(kv, q, B, 1, H, sm_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+mla_status_t mla_verify(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
+                        float sm_scale, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return run_split(kv, q, B, n_q, H, sm_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float sm_scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  g_last_launches = 0;
+  mla_status_t st = check_kv(kv);
+  if (st != MLA_OK) return st;
+  if (T < 0) return MLA_ERR_INVALID_ARG;
+  if (H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_UNSUPPORTED;
+  if (!q || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return MLA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+  if (workspace_bytes < sizeof(mla::WsHeader)) return MLA_ERR_WORKSPACE;
+  if (T == 0) return MLA_OK;
+  mla::AttnParams p = base_params(kv, q, 1, T, H, sm_scale, out, lse);
+  p.hdr = static_cast<mla::WsHeader*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mla::launch_reset_status(p.hdr, s) != cudaSuccess) return MLA_ERR_CUDA;
+  ++g_last_launches;
+  prof_mark(g_prof_start, s);
+  if (mla::launch_attn_v0(p, true, T, s) != cudaSuccess) return MLA_ERR_CUDA;
+  prof_mark(g_prof_stop, s);
+  ++g_last_launches;
+  return MLA_OK;
+}
+
+mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, int64_t R,
+                           void* out, float* lse, void* stream) {
+  g_last_launches = 0;
+  if (S < 0 || R < 0) return MLA_ERR_INVALID_ARG;
+  if (R == 0) return MLA_OK;
+  if (!out || (S > 0 && (!part_out || !part_lse))) return MLA_ERR_INVALID_ARG;
+  if (!aligned(part_out, 16) || !aligned(part_lse, 4) || !aligned(out, 8) ||
+      (lse && !aligned(lse, 4)))
+    return MLA_ERR_INVALID_ARG;
+  if (R > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
+  if (mla::launch_merge_standalone(part_out, part_lse, S, R, static_cast<uint16_t*>(out), lse,
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  ++g_last_launches;
+  return MLA_OK;
+}
+
+mla_status_t mla_read_status(const void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < sizeof(mla::WsHeader)) return MLA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return static_cast<mla_status_t>(word);
+}
+
+const char* mla_status_string(mla_status_t status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: null, negative or misaligned argument";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: heads, positions or page size out of range";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA runtime call failed";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
+    case MLA_ERR_BOUNDS: return "MLA_ERR_BOUNDS: page index outside the pool or length beyond the page table";
+  }
+  return "unknown mla_status_t";
+}
+
+int mla_last_launch_count(void) { return g_last_launches; }
+
+void mla_set_profile_events(void* start, void* stop) {
+  g_prof_start = static_cast<cudaEvent_t>(start);
+  g_prof_stop = static_cast<cudaEvent_t>(stop);
+}
+
+}  // extern "C"
