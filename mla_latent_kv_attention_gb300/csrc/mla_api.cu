@@ -94,9 +94,14 @@ mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
   if (mla::launch_plan(p, mla::kUnitsPerSm * sms, s) != cudaSuccess) return MLA_ERR_CUDA;
   ++g_last_launches;
   prof_mark(g_prof_start, s);
-  if (mla::launch_attn_v0(p, false, 0, s) != cudaSuccess) return MLA_ERR_CUDA;
+  int launched = 0;
+  const cudaError_t e = mla::launch_decode_tc(p, sms, s, &launched);
+  g_last_launches += launched;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   prof_mark(g_prof_stop, s);
-  ++g_last_launches;
   if (mla::launch_merge(p, s) != cudaSuccess) return MLA_ERR_CUDA;
   ++g_last_launches;
   return MLA_OK;
