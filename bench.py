@@ -220,21 +220,25 @@ def bench_ours(args, world, rank, local):
     for e in kst + ksp:  # create the underlying events before handing them to the library
         e.record(stream)
     torch.cuda.synchronize()
-    clocks = ClockSampler(local) if rank == 0 or True else None
+    clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     clocks.mark("t0")
     for i in range(args.steps):
-        mla.mla_set_profile_events(kst[i], ksp[i])
         starts[i].record(stream)
         step(i)
         stops[i].record(stream)
-    mla.mla_set_profile_events(None, None)
     torch.cuda.synchronize()
     clocks.mark("t1")
     barrier(world)
     clk = clocks.stop()
+    # The dominant kernel alone: the same steps again with events around its launch.
+    for i in range(args.steps):
+        mla.mla_set_profile_events(kst[i], ksp[i])
+        step(i)
+    mla.mla_set_profile_events(None, None)
+    torch.cuda.synchronize()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
     kern_ms = [s.elapsed_time(e) for s, e in zip(kst, ksp)]
     ms = sum(step_ms) / len(step_ms)
@@ -280,7 +284,7 @@ def bench_ours(args, world, rank, local):
     line = None
     if rank == 0:
         achieved = nbytes / (kms / 1e3) / 1e9
-        traffic = kernel_traffic("mla_attn_v0.cu")
+        traffic = kernel_traffic("mla_decode_tc.cu")
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -312,12 +316,17 @@ def cpu_baseline(line):
     inp = W.batched_paged_decode()
     nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), 1, inp.H)
     cores = os.cpu_count() or 1
-    t = time.perf_counter()
-    oracle.attention(inp, n_threads=cores)
-    dt = time.perf_counter() - t
+    reps, t0 = 0, time.perf_counter()
+    while True:  # repeat whole passes for about ten seconds of CPU time
+        oracle.attention(inp, n_threads=cores)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 200:
+            break
+    dt = (time.perf_counter() - t0) / reps
     line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores,
-                            "kind": "oracle", "seconds": dt,
-                            "sample": "the whole workload once (32 sequences x 12 heads, float64)"}
+                            "kind": "oracle", "seconds_per_pass": dt, "passes": reps,
+                            "sample": "whole workload (32 sequences x 12 heads, float64), "
+                                      f"{reps} passes"}
 
 
 def main():

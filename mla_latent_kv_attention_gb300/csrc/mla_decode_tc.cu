@@ -26,6 +26,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <math.h>
+#include <stddef.h>
 
 #include "mla_internal.cuh"
 #include "sm100.cuh"
@@ -64,19 +65,27 @@ struct Cfg {
   static constexpr int kOffQ = kOffP + ((kPBytes + 1023) / 1024) * 1024;
   static constexpr int kOffMisc = kOffQ + kQBytes;
   static_assert(kTmemUsed <= 512, "TMEM budget");
+  static_assert(kOffMisc % 16 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0, "alignment");
 };
 
 struct Misc {
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  // float arrays first: they are read as float4 and must be 16-byte aligned
+  alignas(16) float row_scale[48];
+  alignas(16) float red[2][48 * 4];  // per-tile warp maxima, [row][warp]
+  alignas(16) float lred[4][48];
+  alignas(16) float alpha[4][48];    // per-warp copy of this tile's rescale factors
+  alignas(16) int row_j[48];         // new-position index j of each row (very negative for padding)
+  alignas(8) uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full, pv_done, q_full;
   uint64_t wg_bar;  // bounded barrier of the softmax warpgroup (128 arrivals per phase)
   uint32_t tmem_base;
   int abort;
-  float row_scale[48];
-  float red[2][4][48];
-  float lred[4][48];
 };
+static_assert(offsetof(Misc, row_scale) % 16 == 0 && offsetof(Misc, red) % 16 == 0 &&
+                  offsetof(Misc, lred) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0,
+              "vector-accessed arrays must be 16-byte aligned");
+static_assert(offsetof(Misc, kv_full) % 8 == 0, "mbarriers must be 8-byte aligned");
 
 template <int RP>
 constexpr int smem_bytes() {
@@ -119,6 +128,38 @@ __device__ __forceinline__ float2 from_e4m3x2(uint16_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// (lo, hi) -> f16x2 with lo in the low half
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(c) : "r"(h));
+  return c;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)c));
+  return h;
+}
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Byte offset of the 16-byte group `w16` (16 codes, dims 16*w16 .. +15) of term-row n
 // inside the query operand (K-major: four SW128 chunks of 128 dims, then one SW64 chunk).
 template <int NQK>
@@ -145,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* pbuf = smem + C::kOffP;
   uint8_t* qbuf = smem + C::kOffQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_units = p.hdr->num_units;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -161,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ms->q_full, 128);
     mbar_init(&ms->wg_bar, 128);
     ms->abort = 0;
+    for (int r = 0; r < 48; ++r) ms->row_j[r] = (r < args.rows) ? r / args.Hs : -(1 << 30);
     fence_mbar_init();
     prefetch_tensormap(&map_main);
     prefetch_tensormap(&map_tail);
@@ -170,6 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
+  // Everything above overlapped the planner (programmatic dependent launch); from here on
+  // the plan is read. The merge kernel may launch early and waits for this grid itself.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int num_units = p.hdr->num_units;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -212,24 +258,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // Two cursors over this CTA's tiles, polled without blocking: scores (QK) of tile g
+    // may run ahead while values (PV) of tile g-1 wait for their probabilities, and a PV
+    // is issued the moment its P is ready so its KV stage returns to the producer early.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, 128, C::NQK);
       constexpr uint32_t idesc_pv = instr_desc(0, 0, 1, 1, 128, C::NPV);
       const uint32_t q_s = smem_addr(qbuf), p_s = smem_addr(pbuf);
-      uint32_t tile = 0;   // global tile counter (KV stage and S buffer rotation)
-      uint32_t units_done = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++units_done) {
+      auto tiles_of = [&](int u) {
         const Unit un = p.units[u];
-        const int ntiles = (un.key_hi - un.key_lo + kTileKeys - 1) / kTileKeys;
-        if (!(ok = wait_or_abort(&ms->q_full, units_done & 1, ms, p))) break;
-        tc_fence_after();
-        for (int t = 0; t <= ntiles && ok; ++t) {
-          if (t < ntiles) {  // scores of tile t
-            const uint32_t g = tile + t;
-            const int s = g % kStages, sb = g & 1;
-            if (!(ok = wait_or_abort(&ms->kv_full[s], (g / kStages) & 1, ms, p))) break;
-            if (!(ok = wait_or_abort(&ms->s_empty[sb], ((g >> 1) & 1) ^ 1, ms, p))) break;
+        return (un.key_hi - un.key_lo + kTileKeys - 1) / kTileKeys;
+      };
+      // scores cursor
+      int qu = blockIdx.x, qt = 0, qn = (qu < num_units) ? tiles_of(qu) : 0;
+      uint32_t qg = 0, q_units = 0;
+      bool q_ready = false;
+      // values cursor
+      int pu = blockIdx.x, pt = 0, pn = qn;
+      uint32_t pg = 0;
+      uint64_t idle_since = globaltimer_ns();
+      while (pu < num_units) {
+        bool progress = false;
+        if (qu < num_units) {
+          const int s = qg % kStages, sb = qg & 1;
+          bool ready = true;
+          if (qt == 0 && !q_ready) {
+            q_ready = mbar_try_wait(&ms->q_full, q_units & 1);
+            ready = q_ready;
+          }
+          ready = ready && mbar_try_wait(&ms->kv_full[s], (qg / kStages) & 1) &&
+                  mbar_try_wait(&ms->s_empty[sb], ((qg >> 1) & 1) ^ 1);
+          if (ready) {
             tc_fence_after();
             const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
             const uint32_t d = tmem + C::kSCol + sb * C::NQK;
@@ -248,36 +307,57 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_f8f6f4(d, a, b, idesc_qk, 1);
             }
             mma_commit(&ms->s_full[sb]);
+            ++qg;
+            if (++qt == qn) {
+              qu += gridDim.x;
+              qt = 0;
+              q_ready = false;
+              ++q_units;
+              qn = (qu < num_units) ? tiles_of(qu) : 0;
+            }
+            progress = true;
           }
-          if (t > 0) {  // values of tile t-1
-            const uint32_t g = tile + t - 1;
-            const int s = g % kStages;
-            if (!(ok = wait_or_abort(&ms->p_full, g & 1, ms, p))) break;
-            tc_fence_after();
-            const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
+        }
+        if (pg < qg && mbar_try_wait(&ms->p_full, pg & 1)) {
+          tc_fence_after();
+          const int s = pg % kStages;
+          const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
+          const bool first = (pt == 0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint32_t d = tmem + C::kOCol + c * C::OCOLS;
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t d = tmem + C::kOCol + c * C::OCOLS;
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = smem_desc(st + c * kChunkBytes + ks * 4096, kChunkBytes, 1024, Swizzle::k128B);
-                if (C::kStackP) {
-                  const uint64_t b = smem_desc(p_s + ks * 512, 128, 2048, Swizzle::kNone);
-                  mma_f8f6f4(d, a, b, idesc_pv, (t > 1) || ks > 0);
-                } else {
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t a = smem_desc(st + c * kChunkBytes + ks * 4096, kChunkBytes, 1024, Swizzle::k128B);
+              if (C::kStackP) {
+                const uint64_t b = smem_desc(p_s + ks * 512, 128, 2048, Swizzle::kNone);
+                mma_f8f6f4(d, a, b, idesc_pv, !first || ks > 0);
+              } else {
 #pragma unroll
-                  for (int term = 0; term < 3; ++term) {
-                    const uint64_t b = smem_desc(p_s + term * (RP / 16) * 2048 + ks * 512, 128, 2048, Swizzle::kNone);
-                    mma_f8f6f4(d, a, b, idesc_pv, (t > 1) || ks > 0 || term > 0);
-                  }
+                for (int term = 0; term < 3; ++term) {
+                  const uint64_t b = smem_desc(p_s + term * (RP / 16) * 2048 + ks * 512, 128, 2048, Swizzle::kNone);
+                  mma_f8f6f4(d, a, b, idesc_pv, !first || ks > 0 || term > 0);
                 }
               }
             }
-            mma_commit(&ms->kv_empty[s]);
-            mma_commit(&ms->pv_done);
           }
+          mma_commit(&ms->kv_empty[s]);
+          mma_commit(&ms->pv_done);
+          ++pg;
+          if (++pt == pn) {
+            pu += gridDim.x;
+            pt = 0;
+            pn = (pu < num_units) ? tiles_of(pu) : 0;
+          }
+          progress = true;
         }
-        tile += ntiles;
+        if (progress) {
+          idle_since = globaltimer_ns();
+        } else if (globaltimer_ns() - idle_since > kWaitLimitNs || aborted(ms)) {
+          ms->abort = 1;
+          report(p.hdr, MLA_ERR_TIMEOUT);
+          break;
+        }
       }
     }
   } else if (warp >= kSoftmaxWarp0) {
@@ -375,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int L = seq_len_of(p, un.b);
       const int ntiles = (un.key_hi - un.key_lo + kTileKeys - 1) / kTileKeys;
       // last visible key of new position j is L - n_q + j (and the unit ends at key_hi)
-      const int lim0 = min(un.key_hi - 1, L - p.n_q);
       const int lim_cap = un.key_hi - 1;
+      const int lim0 = min(lim_cap, L - p.n_q);
       float m[RP], l[RP];
 #pragma unroll
       for (int r = 0; r < RP; ++r) {
@@ -386,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < ntiles; ++t, ++tile) {
         const int sb = tile & 1;
         const int s = tile % kStages;
-        const int kabs = un.key_lo + t * kTileKeys + i;
+        const int k0 = un.key_lo + t * kTileKeys;
+        const int kabs = k0 + i;
         if (!(ok = wait_or_abort(&ms->s_full[sb], (tile >> 1) & 1, ms, p))) break;
         tc_fence_after();
         float x[RP];
@@ -404,56 +485,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&ms->s_empty[sb]);
-        // scale to log2 units and mask
+        // to log2 units (per-row scale folds sm_scale, kv_scale, the query term scale, log2 e)
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          const int lim = (r < R) ? min(lim_cap, lim0 + r / args.Hs) : -1;
-          x[r] = (kabs <= lim) ? x[r] * ms->row_scale[r] : -INFINITY;
+        for (int r = 0; r < RP; r += 4) {
+          const float4 sc = *reinterpret_cast<const float4*>(&ms->row_scale[r]);
+          x[r] *= sc.x;
+          x[r + 1] *= sc.y;
+          x[r + 2] *= sc.z;
+          x[r + 3] *= sc.w;
         }
-        // tile max per row across the 128 keys
-        float* red = &ms->red[tile & 1][0][0];
+        // masking only on tiles that reach past the first new position's last visible key
+        if (k0 + kTileKeys - 1 > lim0) {
+#pragma unroll
+          for (int r = 0; r < RP; ++r) {
+            const int lim = min(lim_cap, lim0 + ms->row_j[r]);
+            if (kabs > lim) x[r] = -INFINITY;
+          }
+        }
+        // tile max per row: warp max in hardware, then the four warps through shared memory
+        float* red = &ms->red[tile & 1][0];
 #pragma unroll
         for (int r = 0; r < RP; ++r) {
-          float v = x[r];
-          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-          if (lane == 0) red[wq * 48 + r] = v;
+          const float v = warp_max(x[r]);
+          if (lane == 0) red[r * 4 + wq] = v;
         }
         if (!(ok = wg_sync())) break;
-        bool rescale = false;
-        float alpha[RP];
+        bool need_rescale = false;
+        float moff[RP];
 #pragma unroll
         for (int r = 0; r < RP; ++r) {
-          const float tm = fmaxf(fmaxf(red[r], red[48 + r]), fmaxf(red[96 + r], red[144 + r]));
-          const float mn = fmaxf(m[r], tm);
-          alpha[r] = (mn == -INFINITY || m[r] == mn) ? 1.f : exp2f(m[r] - mn);
-          rescale |= (alpha[r] != 1.f);
-          m[r] = mn;
+          const float4 t4 = *reinterpret_cast<const float4*>(&red[r * 4]);
+          const float tm = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
+          float al = 1.f;
+          if (tm > m[r]) {
+            al = ex2(m[r] - tm);  // 0 when m was -inf (nothing accumulated yet)
+            need_rescale |= (m[r] != -INFINITY);
+            l[r] *= al;
+            m[r] = tm;
+          }
+          if (lane == 0) ms->alpha[wq][r] = al;
+          moff[r] = (m[r] == -INFINITY) ? 0.f : m[r] - kPScale;
         }
-        // probabilities as three e4m3 terms (scaled by 2^8), packed per 16 rows
+        // p = 2^(x - m + 8) rounded to fp16, carried exactly by three e4m3 terms
         uint32_t w1[RP / 4], w2[RP / 4], w3[RP / 4];
 #pragma unroll
         for (int r = 0; r < RP; r += 2) {
-          const float p0 = (x[r] == -INFINITY) ? 0.f : exp2f(x[r] - m[r] + kPScale);
-          const float p1 = (x[r + 1] == -INFINITY) ? 0.f : exp2f(x[r + 1] - m[r + 1] + kPScale);
-          const uint16_t c1 = to_e4m3x2(p0, p1);
-          const float2 b1 = from_e4m3x2(c1);
-          const float r0 = p0 - b1.x, r1 = p1 - b1.y;
-          const uint16_t c2 = to_e4m3x2(r0, r1);
-          const float2 b2v = from_e4m3x2(c2);
-          const float q0 = r0 - b2v.x, q1 = r1 - b2v.y;
-          const uint16_t c3 = to_e4m3x2(q0, q1);
-          const float2 b3 = from_e4m3x2(c3);
-          l[r] = l[r] * alpha[r] + (b1.x + b2v.x + b3.x);
-          l[r + 1] = l[r + 1] * alpha[r + 1] + (b1.y + b2v.y + b3.y);
+          const float p0 = ex2(x[r] - moff[r]);
+          const float p1 = ex2(x[r + 1] - moff[r + 1]);
+          l[r] += p0;
+          l[r + 1] += p1;
+          const uint32_t h = f32x2_to_f16x2(p0, p1);
+          const uint32_t c1 = f16x2_to_e4m3x2(h);
+          const uint32_t r1 = hsub2(h, e4m3x2_to_f16x2(c1));
+          const uint32_t c2 = f16x2_to_e4m3x2(r1);
+          const uint32_t r2 = hsub2(r1, e4m3x2_to_f16x2(c2));
+          const uint32_t c3 = f16x2_to_e4m3x2(r2);
           const int wi = r >> 2;
           if ((r & 2) == 0) {
             w1[wi] = c1;
             w2[wi] = c2;
             w3[wi] = c3;
           } else {
-            w1[wi] |= (uint32_t)c1 << 16;
-            w2[wi] |= (uint32_t)c2 << 16;
-            w3[wi] |= (uint32_t)c3 << 16;
+            w1[wi] |= c1 << 16;
+            w2[wi] |= c2 << 16;
+            w3[wi] |= c3 << 16;
           }
         }
         // the previous tile's PV must be done before P and O are touched
@@ -461,7 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_or_abort(&ms->pv_done, pv_waits & 1, ms, p))) break;
           ++pv_waits;
           tc_fence_after();
-          if (rescale) {
+          if (need_rescale) {
+            __syncwarp();
+            const float* al = &ms->alpha[wq][0];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -471,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld16(a, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= alpha[(cc + e) % RP];
+                for (int e = 0; e < 16; ++e) v[e] *= al[(cc + e) % RP];
                 tmem_st16(a, v);
               }
             }
@@ -489,9 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P^T: MN-major, 16 rows x 8 keys core matrices; term t, row group g at
         // (t * RP/16 + g) * 2048, key i at (i / 8) * 128 + (i % 8) * 16.
+        const int off = (i >> 3) * 128 + (i & 7) * 16;
 #pragma unroll
         for (int g = 0; g < RP / 16; ++g) {
-          const int off = (i >> 3) * 128 + (i & 7) * 16;
           *reinterpret_cast<uint4*>(pbuf + (0 * (RP / 16) + g) * 2048 + off) =
               make_uint4(w1[4 * g], w1[4 * g + 1], w1[4 * g + 2], w1[4 * g + 3]);
           *reinterpret_cast<uint4*>(pbuf + (1 * (RP / 16) + g) * 2048 + off) =
@@ -636,8 +733,17 @@ cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensor
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<RP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<RP><<<grid, kThreads, smem, s>>>(a, mm, mt);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<RP>, a, mm, mt);
 }
 
 }  // namespace

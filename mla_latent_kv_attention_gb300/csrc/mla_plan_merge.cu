@@ -72,6 +72,9 @@ __device__ int block_scan(int v, int* scratch, int* total) {
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p, int target_units) {
   __shared__ long long s_ll[32];
   __shared__ int s_i[32];
+  // the attention kernel may start its prologue now; it waits for this grid before
+  // reading the plan
+  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x;
   if (tid == 0) p.hdr->status = 0;  // this call's status word starts clean
   __syncthreads();
@@ -112,45 +115,45 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p, int ta
   }
 }
 
-constexpr int kMergeLanes = 16;    // float4 lanes: 64 dv per CTA
-constexpr int kMergeGroups = 16;   // unit groups per CTA
-constexpr int kMergeThreads = kMergeLanes * kMergeGroups;
-constexpr int kMergeChunks = kDV / (4 * kMergeLanes);  // 8 CTAs per row
+constexpr int kMergeWarps = 4;
+constexpr int kMergeThreads = 32 * kMergeWarps;
+constexpr int kMergeChunks = kDV / 128;  // one CTA per (row, 128-wide dv chunk)
 
-// Merge one 64-wide dv chunk of one row. Partial u of this row sits at
-// po + (base + u * stride) * 512 and pl[base + u * stride].
+// Merge one 128-wide dv chunk of one row. Partial u of the row sits at
+// po + (base + u * stride) * 512 and pl[base + u * stride]. Every thread scans all the
+// lse values itself (they are few and cached); warp w sums partials w, w + 4, ...;
+// lane l owns four consecutive outputs.
 __device__ void merge_chunk(const float* __restrict__ po, const float* __restrict__ pl,
                             int64_t base, int64_t stride, int count, int chunk,
                             uint16_t* __restrict__ out_row, float* lse_out) {
-  __shared__ float s_red[32];
-  __shared__ float4 s_acc[kMergeGroups][kMergeLanes];
-  const int lane = threadIdx.x % kMergeLanes, grp = threadIdx.x / kMergeLanes;
+  __shared__ float4 s_acc[kMergeWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float m = -INFINITY;
-  for (int u = threadIdx.x; u < count; u += blockDim.x) m = fmaxf(m, pl[base + (int64_t)u * stride]);
-  m = block_reduce(m, [](float a, float c) { return fmaxf(a, c); }, s_red);
+  for (int u = 0; u < count; ++u) m = fmaxf(m, pl[base + (int64_t)u * stride]);
   float sum = 0.f;
   if (m != -INFINITY)
-    for (int u = threadIdx.x; u < count; u += blockDim.x) sum += expf(pl[base + (int64_t)u * stride] - m);
-  sum = block_reduce(sum, [](float a, float c) { return a + c; }, s_red);
+    for (int u = 0; u < count; ++u) sum += expf(pl[base + (int64_t)u * stride] - m);
   const float lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (m != -INFINITY) {
-    for (int u = grp; u < count; u += kMergeGroups) {
+#pragma unroll 4
+    for (int u = warp; u < count; u += kMergeWarps) {
       const int64_t r = base + (int64_t)u * stride;
       const float w = expf(pl[r] - lse);
       if (w == 0.f) continue;  // an empty partial (lse = -inf) holds no data worth reading
-      const float4 v = reinterpret_cast<const float4*>(po + r * kDV)[chunk * kMergeLanes + lane];
+      const float4 v = reinterpret_cast<const float4*>(po + r * kDV + chunk * 128)[lane];
       acc.x += w * v.x;
       acc.y += w * v.y;
       acc.z += w * v.z;
       acc.w += w * v.w;
     }
   }
-  s_acc[grp][lane] = acc;
+  s_acc[warp][lane] = acc;
   __syncthreads();
-  if (grp == 0) {
+  if (warp == 0) {
     float4 t = s_acc[0][lane];
-    for (int g = 1; g < kMergeGroups; ++g) {
+#pragma unroll
+    for (int g = 1; g < kMergeWarps; ++g) {
       t.x += s_acc[g][lane].x;
       t.y += s_acc[g][lane].y;
       t.z += s_acc[g][lane].z;
@@ -161,13 +164,15 @@ __device__ void merge_chunk(const float* __restrict__ po, const float* __restric
     uint2 packed;
     packed.x = *reinterpret_cast<unsigned int*>(&lo);
     packed.y = *reinterpret_cast<unsigned int*>(&hi);
-    reinterpret_cast<uint2*>(out_row)[chunk * kMergeLanes + lane] = packed;
+    reinterpret_cast<uint2*>(out_row + chunk * 128)[lane] = packed;
   }
   if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = lse;
 }
 
 // Rows of the decode/verify path whose sequence has more (or fewer) than one unit.
+// Launched as a programmatic dependent of the attention kernel: it waits for that grid.
 __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = blockIdx.x;  // b * R + r
   const int chunk = blockIdx.y;
   const int b = (int)(row / p.R), r = (int)(row % p.R);
@@ -194,9 +199,16 @@ cudaError_t launch_plan(const AttnParams& p, int target_units, cudaStream_t s) {
 }
 
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
-  dim3 grid((unsigned)(p.B * p.R), kMergeChunks);
-  merge_split_kernel<<<grid, kMergeThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.R), kMergeChunks);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_split_kernel, p);
 }
 
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
