@@ -164,6 +164,31 @@ int mla_last_launch_count(void);
  */
 void mla_set_profile_events(void* start, void* stop);
 
+/*
+ * Decode without a caller-provided workspace. (The pages describe no such entry point; it
+ * exists for callers of this library that cannot allocate device memory: an engine that
+ * has already reserved nearly all device memory for its own pools, or a latency-critical
+ * loop where cudaMalloc/cudaFree, which can synchronise the device, are not allowed.)
+ *
+ * Same arguments, layouts and results as mla_decode, but the workspace is a fixed array
+ * of MLA_STATIC_WS_BYTES owned by the library in device memory: every GPU on which the
+ * library's kernels are loaded holds it until the process exits. No memory is allocated
+ * by this call.
+ *  - A batch whose mla_workspace_size(MLA_OP_DECODE, B, H, 1, device) exceeds
+ *    MLA_STATIC_WS_BYTES is rejected with MLA_ERR_WORKSPACE before anything is enqueued
+ *    (16 MiB covers, for example, 32 sequences x 16 heads on a 152-SM GB300).
+ *  - The first call on each device looks up the array's device address (a runtime
+ *    symbol query); make that first call outside any CUDA stream capture.
+ *  - All calls on a device share the one array, which keeps the previous call's
+ *    contents (each call re-plans and overwrites what it reads, and resets its status
+ *    word). Calls whose work overlaps on the GPU (different streams without ordering,
+ *    or several host threads) race on it and give wrong results: serialise them.
+ *  - The device-side status word of these calls cannot be read with mla_read_status.
+ */
+#define MLA_STATIC_WS_BYTES (16u << 20)
+mla_status_t mla_decode_static_ws(const mla_kv_t* kv, const void* q, int B, int H,
+                                  float sm_scale, void* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

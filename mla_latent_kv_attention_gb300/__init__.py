@@ -28,7 +28,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 # Every symbol include/mla.h declares.
 EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse",
            "mla_read_status", "mla_status_string", "mla_last_launch_count",
-           "mla_set_profile_events")
+           "mla_set_profile_events", "mla_decode_static_ws")
 
 
 class MlaError(RuntimeError):
@@ -65,6 +65,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_last_launch_count.argtypes = []
     lib.mla_set_profile_events.argtypes = [P, P]
     lib.mla_set_profile_events.restype = None
+    lib.mla_decode_static_ws.argtypes = [KV, P, i32, i32, f32, P, P, P]
+    lib.mla_decode_static_ws.restype = i32
     for name in ("mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse", "mla_read_status",
                  "mla_last_launch_count"):
         getattr(lib, name).restype = i32

@@ -1,0 +1,63 @@
+"""mla_decode_static_ws: decode for callers that cannot allocate device memory.
+
+Engines that have reserved almost all device memory for their own pools, and hot loops
+that must not call cudaMalloc/cudaFree (which can synchronise the device), cannot hand
+the library a workspace. This entry point runs decode on a fixed workspace the library
+keeps in device memory. The test calls it through the C ABI twice in a row, on two
+different batches so the second call inherits the first call's leftovers in the shared
+workspace, and checks each result against mla_decode with a workspace of its own, within
+the tolerances every parity test here uses. It also checks that a batch too large for
+the fixed workspace is refused before any work is enqueued.
+
+This file is named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_kv_attention_gb300 as mla
+from mla_latent_kv_attention_gb300 import workloads as W
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+def _static_decode(inp, kv):
+    lib = mla.library()
+    q = inp.q[:, 0].contiguous().cuda()
+    out = torch.full((inp.B, inp.H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((inp.B, inp.H), float("nan"), dtype=torch.float32, device="cuda")
+    c = kv.c_struct()
+    status = lib.mla_decode_static_ws(ctypes.byref(c), q.data_ptr(), inp.B, inp.H,
+                                      inp.sm_scale, out.data_ptr(), lse.data_ptr(),
+                                      torch.cuda.current_stream().cuda_stream)
+    assert status == 0, mla.STATUS.get(status, status)
+    return out, lse
+
+
+def test_static_workspace_decode_matches_decode_twice():
+    batches = [
+        W.make_inputs("nalloc_a", [5000, 1200, 64, 3001], H=12, n_q=1, seed=41),
+        W.make_inputs("nalloc_b", [900, 17000], H=16, n_q=1, seed=42),
+    ]
+    for inp in batches:
+        kv = mla.KVCache.from_inputs(inp, "cuda")
+        got_out, got_lse = _static_decode(inp, kv)
+        ref_out, ref_lse = mla.mla_decode(kv, inp.q[:, 0].contiguous().cuda(), inp.sm_scale)
+        torch.cuda.synchronize()
+        compare(got_out, got_lse, ref_out.double().cpu().numpy(),
+                ref_lse.double().cpu().numpy(), f"static workspace {inp.name}")
+
+
+def test_static_workspace_rejects_too_large_batch():
+    lib = mla.library()
+    dev = torch.cuda.current_device()
+    B = 1
+    while mla.mla_workspace_size(mla.MLA_OP_DECODE, B, 16, 1, dev) <= (16 << 20):
+        B *= 2
+    fake = 0x100000  # never touched: the call must fail before enqueuing work
+    kv = mla.mla_kv_t(fake, 1, 64, fake, 1, fake, 1.0)
+    status = lib.mla_decode_static_ws(ctypes.byref(kv), fake, B, 16, 0.1, fake, fake, None)
+    assert status == 3  # MLA_ERR_WORKSPACE
