@@ -41,11 +41,13 @@ constexpr int kStages = 2;
 constexpr int kChunkBytes = 16384;                     // 128 keys x 128 bytes, SW128
 constexpr int kTailOffset = 4 * kChunkBytes;            // 128 keys x 64 bytes, SW64
 constexpr int kStageBytes = kTailOffset + 2 * 4096;     // 73,728
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // producer, MMA, 2 query stagers, 2 softmax warpgroups
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kPScale = 8.0f;                         // P carried as 2^8 * p
+constexpr float kPScale = 4.0f;      // P carried as 2^(x - m + 4): at most 2^8 while x <= m + 4
+constexpr float kRescaleGap = 4.0f;  // the running max (log2 units) moves only past m + 4
+constexpr int kPrefetchTiles = 3;    // tiles the producer pulls into L2 ahead of its TMA loads
 
 template <int RP>
 struct Cfg {
@@ -58,27 +60,33 @@ struct Cfg {
   static constexpr int kTmemUsed = 2 * NQK + 4 * OCOLS;
   static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static constexpr int kQBytes = NQK * kD;
+  // query operand buffers: two (the next unit is staged during this one) when they fit
+  static constexpr int kQB = (RP == 16) ? 2 : 1;
   static constexpr int kPBytes = 3 * RP * kTileKeys;
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffStages = 0;
   static constexpr int kOffP = kStages * kStageBytes;
   static constexpr int kOffQ = kOffP + ((kPBytes + 1023) / 1024) * 1024;
-  static constexpr int kOffMisc = kOffQ + kQBytes;
+  static constexpr int kOffMisc = kOffQ + kQB * kQBytes;
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  static_assert(kOffMisc % 16 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0, "alignment");
+  static_assert(kOffMisc % 16 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0 &&
+                    kQBytes % 1024 == 0, "alignment");
 };
 
 struct Misc {
   // float arrays first: they are read as float4 and must be 16-byte aligned
-  alignas(16) float row_scale[48];
+  alignas(16) float row_scale[2][48];  // by unit parity
   alignas(16) float red[2][48 * 4];  // per-tile warp maxima, [row][warp]
   alignas(16) float lred[4][48];
   alignas(16) float alpha[4][48];    // per-warp copy of this tile's rescale factors
   alignas(16) int row_j[48];         // new-position index j of each row (very negative for padding)
+  alignas(16) int row_off[48];       // j * H + h: the row's index among its sequence's rows
   alignas(8) uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, pv_done, q_full;
-  uint64_t wg_bar;  // bounded barrier of the softmax warpgroup (128 arrivals per phase)
+  uint64_t p_full, pv_done;
+  uint64_t q_full[2];   // query operand buffer holds its unit's terms
+  uint64_t q_empty[2];  // the unit that used the buffer has finished its scores
+  uint64_t wg_bar[2];  // bounded barriers of the two softmax warpgroups (128 arrivals)
   uint32_t tmem_base;
   int abort;
 };
@@ -194,14 +202,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->s_full[s], 1);
-      mbar_init(&ms->s_empty[s], 128);
+      mbar_init(&ms->s_empty[s], 256);
+      mbar_init(&ms->wg_bar[s], 128);
     }
-    mbar_init(&ms->p_full, 128);
+    mbar_init(&ms->p_full, 256);
     mbar_init(&ms->pv_done, 1);
-    mbar_init(&ms->q_full, 128);
-    mbar_init(&ms->wg_bar, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ms->q_full[s], 64);
+      mbar_init(&ms->q_empty[s], 1);
+    }
     ms->abort = 0;
-    for (int r = 0; r < 48; ++r) ms->row_j[r] = (r < args.rows) ? r / args.Hs : -(1 << 30);
+    for (int r = 0; r < 48; ++r) {
+      ms->row_j[r] = (r < args.rows) ? r / args.Hs : -(1 << 30);
+      ms->row_off[r] = (r < args.rows) ? (r / args.Hs) * p.H + args.h0 + r % args.Hs : 0;
+    }
     fence_mbar_init();
     prefetch_tensormap(&map_main);
     prefetch_tensormap(&map_tail);
@@ -223,11 +237,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t rows64 = p.num_pages * (int64_t)p.page_size;
       const int total_rows = rows64 > 0x7fffff00 ? 0x7fffff00 : (int)rows64;
       uint32_t fill = 0;  // tiles issued so far
+      // L2 prefetch cursor: runs kPrefetchTiles tiles ahead of the TMA loads so that they
+      // find their pages in L2 (deeper than the two shared-memory stages allow).
+      int pf_u = blockIdx.x, pf_k = (pf_u < num_units) ? p.units[pf_u].key_lo : 0;
+      uint32_t pf_tiles = 0;
+      auto prefetch_upto = [&](uint32_t target) {
+        while (pf_tiles < target && pf_u < num_units) {
+          const Unit pu = p.units[pf_u];
+          for (int h = 0; h < 2; ++h) {
+            const int kk = pf_k + 64 * h;
+            if (kk < pu.key_hi) {
+              const int phys = p.page_table[(int64_t)pu.b * p.pt_stride + kk / p.page_size];
+              if (phys >= 0 && phys < p.num_pages) {
+                const int rows = min(64, pu.key_hi - kk);
+                bulk_prefetch_l2(p.pool + ((int64_t)phys * p.page_size + kk % p.page_size) * kD,
+                                 (uint32_t)rows * kD);
+              }
+            }
+          }
+          ++pf_tiles;
+          pf_k += kTileKeys;
+          if (pf_k >= pu.key_hi) {
+            pf_u += gridDim.x;
+            if (pf_u < num_units) pf_k = p.units[pf_u].key_lo;
+          }
+        }
+      };
       for (int u = blockIdx.x; u < num_units && !aborted(ms); u += gridDim.x) {
         const Unit un = p.units[u];
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
           const int s = fill % kStages;
           const uint32_t n = fill / kStages;
+          prefetch_upto(fill + 1 + kPrefetchTiles);
           if (!wait_or_abort(&ms->kv_empty[s], (n & 1) ^ 1, ms, p)) break;
           uint8_t* st = smem + C::kOffStages + s * kStageBytes;
           mbar_arrive_expect_tx(&ms->kv_full[s], kStageBytes);
@@ -264,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, 128, C::NQK);
       constexpr uint32_t idesc_pv = instr_desc(0, 0, 1, 1, 128, C::NPV);
-      const uint32_t q_s = smem_addr(qbuf), p_s = smem_addr(pbuf);
+      const uint32_t q_s0 = smem_addr(qbuf), p_s = smem_addr(pbuf);
       auto tiles_of = [&](int u) {
         const Unit un = p.units[u];
         return (un.key_hi - un.key_lo + kTileKeys - 1) / kTileKeys;
@@ -279,46 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t idle_since = globaltimer_ns();
       while (pu < num_units) {
         bool progress = false;
-        if (qu < num_units) {
-          const int s = qg % kStages, sb = qg & 1;
-          bool ready = true;
-          if (qt == 0 && !q_ready) {
-            q_ready = mbar_try_wait(&ms->q_full, q_units & 1);
-            ready = q_ready;
-          }
-          ready = ready && mbar_try_wait(&ms->kv_full[s], (qg / kStages) & 1) &&
-                  mbar_try_wait(&ms->s_empty[sb], ((qg >> 1) & 1) ^ 1);
-          if (ready) {
-            tc_fence_after();
-            const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
-            const uint32_t d = tmem + C::kSCol + sb * C::NQK;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = smem_desc(st + c * kChunkBytes + kk * 32, 16, 1024, Swizzle::k128B);
-                const uint64_t b = smem_desc(q_s + c * (C::NQK * 128) + kk * 32, 16, 1024, Swizzle::k128B);
-                mma_f8f6f4(d, a, b, idesc_qk, (c | kk) != 0);
-              }
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const uint64_t a = smem_desc(st + kTailOffset + kk * 32, 16, 512, Swizzle::k64B);
-              const uint64_t b = smem_desc(q_s + 4 * (C::NQK * 128) + kk * 32, 16, 512, Swizzle::k64B);
-              mma_f8f6f4(d, a, b, idesc_qk, 1);
-            }
-            mma_commit(&ms->s_full[sb]);
-            ++qg;
-            if (++qt == qn) {
-              qu += gridDim.x;
-              qt = 0;
-              q_ready = false;
-              ++q_units;
-              qn = (qu < num_units) ? tiles_of(qu) : 0;
-            }
-            progress = true;
-          }
-        }
-        if (pg < qg && mbar_try_wait(&ms->p_full, pg & 1)) {
+        // values first: a finished PV hands its KV stage back to the producer
+        if (pg < qg && mbar_test_wait(&ms->p_full, pg & 1)) {
           tc_fence_after();
           const int s = pg % kStages;
           const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
@@ -351,115 +354,197 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           progress = true;
         }
+        if (qu < num_units) {
+          const int s = qg % kStages, sb = qg & 1;
+          bool ready = true;
+          const int qslot = q_units % C::kQB;
+          if (qt == 0 && !q_ready) {
+            q_ready = mbar_test_wait(&ms->q_full[qslot], (q_units / C::kQB) & 1);
+            ready = q_ready;
+          }
+          ready = ready && mbar_test_wait(&ms->kv_full[s], (qg / kStages) & 1) &&
+                  mbar_test_wait(&ms->s_empty[sb], ((qg >> 1) & 1) ^ 1);
+          if (ready) {
+            tc_fence_after();
+            const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
+            const uint32_t d = tmem + C::kSCol + sb * C::NQK;
+            const uint32_t q_s = q_s0 + qslot * C::kQBytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = smem_desc(st + c * kChunkBytes + kk * 32, 16, 1024, Swizzle::k128B);
+                const uint64_t b = smem_desc(q_s + c * (C::NQK * 128) + kk * 32, 16, 1024, Swizzle::k128B);
+                mma_f8f6f4(d, a, b, idesc_qk, (c | kk) != 0);
+              }
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint64_t a = smem_desc(st + kTailOffset + kk * 32, 16, 512, Swizzle::k64B);
+              const uint64_t b = smem_desc(q_s + 4 * (C::NQK * 128) + kk * 32, 16, 512, Swizzle::k64B);
+              mma_f8f6f4(d, a, b, idesc_qk, 1);
+            }
+            mma_commit(&ms->s_full[sb]);
+            ++qg;
+            if (++qt == qn) {
+              mma_commit(&ms->q_empty[qslot]);  // that query buffer is free once these complete
+              qu += gridDim.x;
+              qt = 0;
+              q_ready = false;
+              ++q_units;
+              qn = (qu < num_units) ? tiles_of(qu) : 0;
+            }
+            progress = true;
+          }
+        }
         if (progress) {
           idle_since = globaltimer_ns();
         } else if (globaltimer_ns() - idle_since > kWaitLimitNs || aborted(ms)) {
           ms->abort = 1;
           report(p.hdr, MLA_ERR_TIMEOUT);
           break;
+        } else {
+          __nanosleep(40);  // leave the issue slots to the softmax warp on this SMSP
         }
       }
     }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------------ query stager
+    // Each unit's query rows go into the query operand as two e4m3 terms with a per-row
+    // power-of-two scale, as soon as the previous unit's scores stopped reading it; the
+    // softmax warps meanwhile finish the previous unit.
+    const int w2 = warp - 2;
+    const int R = args.rows;
+    const float kv_scale = p.kv_scale;
+    uint32_t k = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++k) {
+      const int slot = k % C::kQB;
+      if (k >= (uint32_t)C::kQB && !wait_or_abort(&ms->q_empty[slot], ((k / C::kQB) - 1) & 1, ms, p)) break;
+      uint8_t* qdst = qbuf + slot * C::kQBytes;
+      float* row_scale = ms->row_scale[k & 1];
+      const uint16_t* qseq = p.q + (int64_t)p.units[u].b * p.R * kD;
+      // rows r0, r0+2, r0+4, r0+6 of this warp: all loads first, then the arithmetic
+      for (int r0 = w2; r0 < RP; r0 += 8) {
+        uint4 ld[4][2], tl[4][2];
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int r = r0 + 2 * k2;
+          ld[k2][0] = ld[k2][1] = tl[k2][0] = tl[k2][1] = make_uint4(0, 0, 0, 0);
+          if (r < R) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(qseq + (int64_t)ms->row_off[r] * kD);
+            ld[k2][0] = s4[2 * lane];
+            ld[k2][1] = s4[2 * lane + 1];
+            if (lane < 4) {  // dims 512 + 16*lane .. +15 (1024 bytes in: 64 uint4)
+              tl[k2][0] = s4[64 + 2 * lane];
+              tl[k2][1] = s4[64 + 2 * lane + 1];
+            }
+          }
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int r = r0 + 2 * k2;
+          if (r >= RP) break;
+          const bool real = r < R;
+          float v[16], tail[16];
+          {
+            const uint32_t w[8] = {ld[k2][0].x, ld[k2][0].y, ld[k2][0].z, ld[k2][0].w,
+                                   ld[k2][1].x, ld[k2][1].y, ld[k2][1].z, ld[k2][1].w};
+            const uint32_t wt[8] = {tl[k2][0].x, tl[k2][0].y, tl[k2][0].z, tl[k2][0].w,
+                                    tl[k2][1].x, tl[k2][1].y, tl[k2][1].z, tl[k2][1].w};
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              v[e] = __uint_as_float((w[e >> 1] >> ((e & 1) * 16)) << 16);
+              tail[e] = __uint_as_float((wt[e >> 1] >> ((e & 1) * 16)) << 16);
+            }
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fmaxf(fabsf(v[e]), fabsf(tail[e])));
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          // scale 2^ex so that amax * 2^ex lies in (224, 448]; from the exponent field of
+          // amax (normal floats: biased exponent E means amax in [2^(E-127), 2^(E-126)))
+          int ex = 0;
+          if (amax >= 1.17549435e-38f && amax <= 3.4e38f) {
+            const int E = (__float_as_int(amax) >> 23) & 0xFF;
+            ex = 135 - E;  // amax * 2^ex in [256, 512)
+            if (amax * __int_as_float((127 + ex) << 23) > 448.f) ex -= 1;
+            ex = max(-126, min(126, ex));  // both 2^ex and 2^-ex stay normal floats
+          }
+          const float up = __int_as_float((127 + ex) << 23);    // 2^ex, exact
+          const float down = __int_as_float((127 - ex) << 23);  // 2^-ex, exact
+          if (lane == 0) row_scale[r] = real ? p.sm_scale * kv_scale * down * kLog2e : 0.f;
+          // two terms per value, packed 16 codes per 16-byte group
+          auto emit = [&](const float* x, int w16) {
+            uint32_t t1w[4], t2w[4];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float a0 = x[e] * up, a1 = x[e + 1] * up;
+              const uint16_t c1 = to_e4m3x2(a0, a1);
+              const float2 b1 = from_e4m3x2(c1);
+              const uint16_t c2 = to_e4m3x2(a0 - b1.x, a1 - b1.y);
+              const int wi = e >> 2, sh = (e & 2) * 8;
+              if ((e & 2) == 0) {
+                t1w[wi] = c1;
+                t2w[wi] = c2;
+              } else {
+                t1w[wi] |= (uint32_t)c1 << sh;
+                t2w[wi] |= (uint32_t)c2 << sh;
+              }
+            }
+            *reinterpret_cast<uint4*>(qdst + q_offset<C::NQK>(r, w16)) = make_uint4(t1w[0], t1w[1], t1w[2], t1w[3]);
+            *reinterpret_cast<uint4*>(qdst + q_offset<C::NQK>(RP + r, w16)) = make_uint4(t2w[0], t2w[1], t2w[2], t2w[3]);
+          };
+          emit(v, lane);
+          if (lane < 4) emit(tail, 32 + lane);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&ms->q_full[slot]);
+    }
   } else if (warp >= kSoftmaxWarp0) {
-    // ------------------------------------------------------------------ softmax warpgroup
-    const int wq = warp - kSoftmaxWarp0;  // TMEM lane quadrant
-    const int i = wq * 32 + lane;         // key within the tile == TMEM lane
+    // ------------------------------------------------------------------ softmax warpgroups
+    // Two warpgroups, each owning half of the query rows; thread i of a warpgroup owns key
+    // i of the tile (its TMEM lane).
+    constexpr int RH = RP / 2;
+    const int wg = (warp - kSoftmaxWarp0) >> 2;
+    const int rb = wg * RH;  // rows [rb, rb + RH)
+    const int wq = warp & 3;  // TMEM lane quadrant
+    const int i = wq * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
     const int R = args.rows;
     const float kv_scale = p.kv_scale;
-    uint32_t tile = 0, pv_waits = 0, wg_phase = 0;
+    uint32_t tile = 0, pv_waits = 0, wg_phase = 0, k = 0;
+    uint64_t* wg_bar = &ms->wg_bar[wg];
     // Bounded warpgroup barrier: every thread arrives, then waits for the phase.
     auto wg_sync = [&]() -> bool {
-      mbar_arrive(&ms->wg_bar);
-      const bool good = wait_or_abort(&ms->wg_bar, wg_phase & 1, ms, p);
+      mbar_arrive(wg_bar);
+      const bool good = wait_or_abort(wg_bar, wg_phase & 1, ms, p);
       ++wg_phase;
       return good;
     };
-
-    // Stage the query rows of unit u as two e4m3 terms with a per-row power-of-two scale.
-    auto stage_q = [&](int u) {
-      const Unit un = p.units[u];
-      for (int r = wq; r < RP; r += 4) {
-        float v[18];
-        float amax = 0.f;
-        const bool real = r < R;
-        const int j = real ? r / args.Hs : 0, h = real ? args.h0 + r % args.Hs : 0;
-        const uint16_t* src = p.q + (((int64_t)un.b * p.n_q + j) * p.H + h) * kD;
-        // lane holds dims [16*lane, 16*lane+16) and, for lane < 4, [512 + 16*lane, ...)
-#pragma unroll
-        for (int e = 0; e < 18; ++e) v[e] = 0.f;
-        if (real) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(src);
-          uint4 a = s4[2 * lane], bq = s4[2 * lane + 1];
-          uint32_t w[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = __uint_as_float((w[e >> 1] >> ((e & 1) * 16)) << 16);
-        }
-        float tail[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) tail[e] = 0.f;
-        if (real && lane < 4) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(src + 512);
-          uint4 a = s4[2 * lane], bq = s4[2 * lane + 1];
-          uint32_t w[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-          for (int e = 0; e < 16; ++e) tail[e] = __uint_as_float((w[e >> 1] >> ((e & 1) * 16)) << 16);
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fmaxf(fabsf(v[e]), fabsf(tail[e])));
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        // scale 2^e so that amax * 2^e lies in (224, 448]
-        int ex = 0;
-        if (amax > 0.f && isfinite(amax)) {
-          int fe;
-          frexpf(amax, &fe);           // amax = f * 2^fe, f in [0.5, 1)
-          ex = 9 - fe;                 // amax * 2^ex in [256, 512) ... adjust below
-          if (ldexpf(amax, ex) > 448.f) ex -= 1;
-        }
-        if (lane == 0) ms->row_scale[r] = real ? p.sm_scale * kv_scale * ldexpf(1.f, -ex) * kLog2e : 0.f;
-        // two terms per value, packed 16 codes per 16-byte group
-        auto emit = [&](const float* x, int w16) {
-          uint32_t t1w[4], t2w[4];
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float a0 = ldexpf(x[e], ex), a1 = ldexpf(x[e + 1], ex);
-            const uint16_t c1 = to_e4m3x2(a0, a1);
-            const float2 b1 = from_e4m3x2(c1);
-            const uint16_t c2 = to_e4m3x2(a0 - b1.x, a1 - b1.y);
-            const int wi = e >> 2, sh = (e & 2) * 8;
-            if ((e & 2) == 0) {
-              t1w[wi] = c1;
-              t2w[wi] = c2;
-            } else {
-              t1w[wi] |= (uint32_t)c1 << sh;
-              t2w[wi] |= (uint32_t)c2 << sh;
-            }
-          }
-          *reinterpret_cast<uint4*>(qbuf + q_offset<C::NQK>(r, w16)) = make_uint4(t1w[0], t1w[1], t1w[2], t1w[3]);
-          *reinterpret_cast<uint4*>(qbuf + q_offset<C::NQK>(RP + r, w16)) = make_uint4(t2w[0], t2w[1], t2w[2], t2w[3]);
-        };
-        emit(v, lane);
-        if (lane < 4) emit(tail, 32 + lane);
-      }
-      fence_proxy_async_smem();
-      const bool good = wg_sync();  // row_scale visible to the whole warpgroup
-      mbar_arrive(&ms->q_full);
-      return good;
-    };
-
     bool ok = true;
-    if (blockIdx.x < num_units) ok = stage_q(blockIdx.x);
-
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++k) {
       const Unit un = p.units[u];
       const int L = seq_len_of(p, un.b);
       const int ntiles = (un.key_hi - un.key_lo + kTileKeys - 1) / kTileKeys;
+      const bool final_out = p.seqs[un.b].count == 1;
+      if (wg == 0) {  // warm L2 with the next unit's query rows (9 lines of 128 bytes per row)
+        const int un_next = u + gridDim.x;
+        if (un_next < num_units) {
+          const int bn = p.units[un_next].b;
+          if (bn != un.b)
+            for (int x = i; x < R * 9; x += 128)
+              prefetch_l2(reinterpret_cast<const uint8_t*>(p.q + ((int64_t)bn * p.R + ms->row_off[x / 9]) * kD) + (x % 9) * 128);
+        }
+      }
       // last visible key of new position j is L - n_q + j (and the unit ends at key_hi)
       const int lim_cap = un.key_hi - 1;
       const int lim0 = min(lim_cap, L - p.n_q);
-      float m[RP], l[RP];
+      // this unit's row scales (staged with its query terms)
+      if (!(ok = wait_or_abort(&ms->q_full[k % C::kQB], (k / C::kQB) & 1, ms, p))) break;
+      float rs[RH], m[RH], l[RH];
 #pragma unroll
-      for (int r = 0; r < RP; ++r) {
+      for (int r = 0; r < RH; ++r) {
+        rs[r] = ms->row_scale[k & 1][rb + r];
         m[r] = -INFINITY;
         l[r] = 0.f;
       }
@@ -470,66 +555,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kabs = k0 + i;
         if (!(ok = wait_or_abort(&ms->s_full[sb], (tile >> 1) & 1, ms, p))) break;
         tc_fence_after();
-        float x[RP];
+        float x[RH];
         {
-          const uint32_t base = tmem + lane_addr + C::kSCol + sb * C::NQK;
+          const uint32_t base = tmem + lane_addr + C::kSCol + sb * C::NQK + rb;
 #pragma unroll
-          for (int c = 0; c < RP; c += 16) {
-            float a[16], b2[16];
-            tmem_ld16(base + c, a);
-            tmem_ld16(base + RP + c, b2);
+          for (int c = 0; c < RH; c += 8) {
+            float a[8], b2[8];
+            tmem_ld8(base + c, a);
+            tmem_ld8(base + RP + c, b2);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x[c + e] = a[e] + b2[e];
+            for (int e = 0; e < 8; ++e) x[c + e] = (a[e] + b2[e]) * rs[c + e];
           }
         }
         tc_fence_before();
         mbar_arrive(&ms->s_empty[sb]);
-        // to log2 units (per-row scale folds sm_scale, kv_scale, the query term scale, log2 e)
-#pragma unroll
-        for (int r = 0; r < RP; r += 4) {
-          const float4 sc = *reinterpret_cast<const float4*>(&ms->row_scale[r]);
-          x[r] *= sc.x;
-          x[r + 1] *= sc.y;
-          x[r + 2] *= sc.z;
-          x[r + 3] *= sc.w;
-        }
         // masking only on tiles that reach past the first new position's last visible key
         if (k0 + kTileKeys - 1 > lim0) {
 #pragma unroll
-          for (int r = 0; r < RP; ++r) {
-            const int lim = min(lim_cap, lim0 + ms->row_j[r]);
+          for (int r = 0; r < RH; ++r) {
+            const int lim = min(lim_cap, lim0 + ms->row_j[rb + r]);
             if (kabs > lim) x[r] = -INFINITY;
           }
         }
         // tile max per row: warp max in hardware, then the four warps through shared memory
         float* red = &ms->red[tile & 1][0];
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
+        for (int r = 0; r < RH; ++r) {
           const float v = warp_max(x[r]);
-          if (lane == 0) red[r * 4 + wq] = v;
+          if (lane == 0) red[(rb + r) * 4 + wq] = v;
         }
         if (!(ok = wg_sync())) break;
         bool need_rescale = false;
-        float moff[RP];
+        float moff[RH];
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          const float4 t4 = *reinterpret_cast<const float4*>(&red[r * 4]);
+        for (int r = 0; r < RH; ++r) {
+          const float4 t4 = *reinterpret_cast<const float4*>(&red[(rb + r) * 4]);
           const float tm = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
           float al = 1.f;
-          if (tm > m[r]) {
+          if (tm > m[r] + kRescaleGap) {  // lazy: small increases are absorbed by the 2^8 headroom
             al = ex2(m[r] - tm);  // 0 when m was -inf (nothing accumulated yet)
             need_rescale |= (m[r] != -INFINITY);
             l[r] *= al;
             m[r] = tm;
           }
-          if (lane == 0) ms->alpha[wq][r] = al;
+          if (lane == 0) ms->alpha[wq][rb + r] = al;
           moff[r] = (m[r] == -INFINITY) ? 0.f : m[r] - kPScale;
         }
-        // p = 2^(x - m + 8) rounded to fp16, carried exactly by three e4m3 terms
-        uint32_t w1[RP / 4], w2[RP / 4], w3[RP / 4];
+        // p = 2^(x - m + 4) <= 2^8 rounded to fp16, carried exactly by three e4m3 terms
+        uint32_t w1[RH / 4], w2[RH / 4], w3[RH / 4];
 #pragma unroll
-        for (int r = 0; r < RP; r += 2) {
+        for (int r = 0; r < RH; r += 2) {
           const float p0 = ex2(x[r] - moff[r]);
           const float p1 = ex2(x[r + 1] - moff[r + 1]);
           l[r] += p0;
@@ -558,25 +634,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (need_rescale) {
             __syncwarp();
-            const float* al = &ms->alpha[wq][0];
+            const float* al = &ms->alpha[wq][rb];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
-              for (int cc = 0; cc < C::OCOLS; cc += 16) {
-                const uint32_t a = tmem + lane_addr + C::kOCol + c * C::OCOLS + cc;
-                float v[16];
-                tmem_ld16(a, v);
-                tmem_wait_ld();
+              for (int term = 0; term < (C::kStackP ? 3 : 1); ++term) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= al[(cc + e) % RP];
-                tmem_st16(a, v);
+                for (int cc = 0; cc < RH; cc += 8) {
+                  const uint32_t a = tmem + lane_addr + C::kOCol + c * C::OCOLS + term * RP + rb + cc;
+                  float v[8];
+                  tmem_ld8(a, v);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) v[e] *= al[cc + e];
+                  tmem_st8(a, v);
+                }
               }
             }
             tmem_wait_st();
           }
         }
         // keys past this unit's range: zero their V bytes so 0 * garbage cannot be NaN
-        if (kabs >= un.key_hi) {
+        if (wg == 0 && kabs >= un.key_hi) {
           uint8_t* st = smem + C::kOffStages + s * kStageBytes + (i >> 6) * 8192 + (i & 63) * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -585,86 +664,86 @@ __global__ void __launch_bounds__(kThreads, 1)
               reinterpret_cast<uint4*>(st + c * kChunkBytes)[e] = make_uint4(0, 0, 0, 0);
         }
         // P^T: MN-major, 16 rows x 8 keys core matrices; term t, row group g at
-        // (t * RP/16 + g) * 2048, key i at (i / 8) * 128 + (i % 8) * 16.
+        // (t * RP/16 + g) * 2048, key i at (i / 8) * 128 + (i % 8) * 16, row r at byte r % 16.
+        // This warpgroup writes its rows 8 at a time (8-byte halves of the 16-byte rows).
         const int off = (i >> 3) * 128 + (i & 7) * 16;
 #pragma unroll
-        for (int g = 0; g < RP / 16; ++g) {
-          *reinterpret_cast<uint4*>(pbuf + (0 * (RP / 16) + g) * 2048 + off) =
-              make_uint4(w1[4 * g], w1[4 * g + 1], w1[4 * g + 2], w1[4 * g + 3]);
-          *reinterpret_cast<uint4*>(pbuf + (1 * (RP / 16) + g) * 2048 + off) =
-              make_uint4(w2[4 * g], w2[4 * g + 1], w2[4 * g + 2], w2[4 * g + 3]);
-          *reinterpret_cast<uint4*>(pbuf + (2 * (RP / 16) + g) * 2048 + off) =
-              make_uint4(w3[4 * g], w3[4 * g + 1], w3[4 * g + 2], w3[4 * g + 3]);
+        for (int blk = 0; blk < RH / 8; ++blk) {
+          const int row0 = rb + 8 * blk;
+          const int o = (row0 >> 4) * 2048 + off + ((row0 & 15) >> 3) * 8;
+          *reinterpret_cast<uint2*>(pbuf + 0 * (RP / 16) * 2048 + o) = make_uint2(w1[2 * blk], w1[2 * blk + 1]);
+          *reinterpret_cast<uint2*>(pbuf + 1 * (RP / 16) * 2048 + o) = make_uint2(w2[2 * blk], w2[2 * blk + 1]);
+          *reinterpret_cast<uint2*>(pbuf + 2 * (RP / 16) * 2048 + o) = make_uint2(w3[2 * blk], w3[2 * blk + 1]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&ms->p_full);
       }
       if (!ok) break;
-      // next unit's queries can go in now: all QK of this unit are complete
-      const int un_next = u + gridDim.x;
-      if (un_next < num_units && !(ok = stage_q(un_next))) break;
       // ---- epilogue: row sums, then O / l
-      float* lred = &ms->lred[0][0];
 #pragma unroll
-      for (int r = 0; r < RP; ++r) {
+      for (int r = 0; r < RH; ++r) {
         float v = l[r];
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) lred[wq * 48 + r] = v;
+        if (lane == 0) ms->lred[wq][rb + r] = v;
       }
       if (!(ok = wg_sync())) break;
-      float inv[RP];
+      float inv[RH];
 #pragma unroll
-      for (int r = 0; r < RP; ++r) {
-        const float lt = lred[r] + lred[48 + r] + lred[96 + r] + lred[144 + r];
+      for (int r = 0; r < RH; ++r) {
+        const int rr = rb + r;
+        const float lt = ms->lred[0][rr] + ms->lred[1][rr] + ms->lred[2][rr] + ms->lred[3][rr];
         l[r] = lt;
         inv[r] = lt > 0.f ? kv_scale / lt : 0.f;
       }
       if (!(ok = wait_or_abort(&ms->pv_done, pv_waits & 1, ms, p))) break;
       ++pv_waits;
       tc_fence_after();
-      const bool final_out = p.seqs[un.b].count == 1;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float o[C::OCOLS];
+        constexpr int NT = C::kStackP ? 3 : 1;
+        float o[NT][RH];
 #pragma unroll
-        for (int cc = 0; cc < C::OCOLS; cc += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_addr + C::kOCol + c * C::OCOLS + cc, v);
+        for (int term = 0; term < NT; ++term)
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[cc + e] = v[e];
-        }
+          for (int cc = 0; cc < RH; cc += 8) {
+            float v[8];
+            tmem_ld8(tmem + lane_addr + C::kOCol + c * C::OCOLS + term * RP + rb + cc, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[term][cc + e] = v[e];
+          }
         tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          if (r >= R) break;
-          float acc = o[r];
-          if (C::kStackP) acc += o[RP + r] + o[2 * RP + r];
-          const int j = r / args.Hs, h = args.h0 + r % args.Hs;
-          const int64_t orow = ((int64_t)un.b * p.n_q + j) * p.H + h;
+        for (int r = 0; r < RH; ++r) {
+          if (rb + r >= R) break;
+          float acc = o[0][r];
+#pragma unroll
+          for (int term = 1; term < NT; ++term) acc += o[term][r];
           const int dv = c * 128 + i;
+          const int roff = ms->row_off[rb + r];
           if (final_out) {
-            p.out[orow * kDV + dv] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv[r]));
+            p.out[((int64_t)un.b * p.R + roff) * kDV + dv] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv[r]));
           } else {
-            p.part_out[((int64_t)u * p.R + j * p.H + h) * kDV + dv] = acc * inv[r];
+            p.part_out[((int64_t)u * p.R + roff) * kDV + dv] = acc * inv[r];
           }
         }
       }
       tc_fence_before();
-      if (i < R) {
+      if (i < RH && rb + i < R) {
         float lt = 0.f, mm = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < RP; ++r)
+        for (int r = 0; r < RH; ++r)
           if (r == i) {
             lt = l[r];
             mm = m[r];
           }
         const float lse = (lt > 0.f) ? 0.6931471805599453f * (mm - kPScale + log2f(lt)) : -INFINITY;
-        const int j = i / args.Hs, h = args.h0 + i % args.Hs;
+        const int roff = ms->row_off[rb + i];
         if (final_out) {
-          if (p.lse) p.lse[((int64_t)un.b * p.n_q + j) * p.H + h] = lse;
+          if (p.lse) p.lse[(int64_t)un.b * p.R + roff] = lse;
         } else {
-          p.part_lse[(int64_t)u * p.R + j * p.H + h] = lse;
+          p.part_lse[(int64_t)u * p.R + roff] = lse;
         }
       }
     }

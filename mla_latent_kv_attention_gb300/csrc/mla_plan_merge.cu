@@ -76,6 +76,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p, int ta
   // reading the plan
   asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x;
+  // Warm L2 with every query row while the memory system is still quiet: the attention
+  // kernel stages them right when its KV stream starts, and then they would queue behind it.
+  {
+    const char* q = reinterpret_cast<const char*>(p.q);
+    const int64_t lines = (int64_t)p.B * p.R * (kD * 2 / 128);
+    for (int64_t x = tid; x < lines; x += blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(q + x * 128));
+  }
   if (tid == 0) p.hdr->status = 0;  // this call's status word starts clean
   __syncthreads();
   long long blocks = 0;
@@ -129,10 +137,13 @@ __device__ void merge_chunk(const float* __restrict__ po, const float* __restric
   __shared__ float4 s_acc[kMergeWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float m = -INFINITY;
+#pragma unroll 8
   for (int u = 0; u < count; ++u) m = fmaxf(m, pl[base + (int64_t)u * stride]);
   float sum = 0.f;
-  if (m != -INFINITY)
+  if (m != -INFINITY) {
+#pragma unroll 8
     for (int u = 0; u < count; ++u) sum += expf(pl[base + (int64_t)u * stride] - m);
+  }
   const float lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (m != -INFINITY) {
