@@ -149,15 +149,24 @@ mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float 
   if (!workspace || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
   if (workspace_bytes < sizeof(mla::WsHeader)) return MLA_ERR_WORKSPACE;
   if (T == 0) return MLA_OK;
+  int dev;
+  if ((st = current_device(&dev)) != MLA_OK) return st;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return MLA_ERR_CUDA;
   mla::AttnParams p = base_params(kv, q, 1, T, H, sm_scale, out, lse);
   p.hdr = static_cast<mla::WsHeader*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (mla::launch_reset_status(p.hdr, s) != cudaSuccess) return MLA_ERR_CUDA;
   ++g_last_launches;
   prof_mark(g_prof_start, s);
-  if (mla::launch_attn_v0(p, true, T, s) != cudaSuccess) return MLA_ERR_CUDA;
+  int launched = 0;
+  const cudaError_t e = mla::launch_prefill_tc(p, sms, s, &launched);
+  g_last_launches += launched;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   prof_mark(g_prof_stop, s);
-  ++g_last_launches;
   return MLA_OK;
 }
 

@@ -103,8 +103,19 @@ constexpr int smem_bytes() {
 struct DecodeArgs {
   AttnParams p;
   int h0, Hs;  // heads [h0, h0 + Hs) handled by this launch
-  int rows;    // n_q * Hs (<= RP)
-  int total_rows_alloc;
+  int rows;    // rows per unit: n_q * Hs (decode/verify) or P * H (prefill), <= RP
+  int prefill;    // 1: units are blocks of P new positions of one sequence (no planner)
+  int P;          // prefill: new positions per unit
+  int num_units;  // prefill: ceil(n_q / P)
+};
+
+// One unit of work as every role of the kernel sees it.
+struct UnitInfo {
+  int b, key_lo, key_hi;
+  int qrow0;      // global row (of q, out, lse) of the unit's row 0
+  int j0;         // new-position index of the unit's first position
+  int rows;       // valid rows of the unit
+  int final_out;  // 1: bf16 out + lse directly; 0: normalised partial for the merge
 };
 
 __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
@@ -113,6 +124,38 @@ __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
   if (L < 0) return 0;
   if ((int64_t)L > cap) return (int)cap;
   return L;
+}
+
+__device__ __forceinline__ UnitInfo get_unit(const DecodeArgs& a, int num_units, int u) {
+  const AttnParams& p = a.p;
+  UnitInfo x;
+  if (!a.prefill) {
+    const Unit un = p.units[u];
+    x.b = un.b;
+    x.key_lo = un.key_lo;
+    x.key_hi = un.key_hi;
+    x.qrow0 = un.b * p.R;
+    x.j0 = 0;
+    x.rows = a.rows;
+    x.final_out = p.seqs[un.b].count == 1;
+  } else {
+    // the last positions see the most keys: hand those out first
+    const int pos0 = (num_units - 1 - u) * a.P;
+    const int npos = min(a.P, p.n_q - pos0);
+    const int L = seq_len_of(p, 0);
+    x.b = 0;
+    x.key_lo = 0;
+    x.key_hi = max(0, min(L, L - p.n_q + pos0 + npos));  // last key the unit's last position sees, + 1
+    x.qrow0 = pos0 * p.H;
+    x.j0 = pos0;
+    x.rows = npos * p.H;
+    x.final_out = 1;
+  }
+  return x;
+}
+
+__device__ __forceinline__ int tiles_in(const UnitInfo& x) {
+  return (x.key_hi - x.key_lo + kTileKeys - 1) / kTileKeys;
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Misc* m,
@@ -229,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the plan is read. The merge kernel may launch early and waits for this grid itself.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int num_units = p.hdr->num_units;
+  const int num_units = args.prefill ? args.num_units : p.hdr->num_units;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -239,11 +282,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fill = 0;  // tiles issued so far
       // L2 prefetch cursor: runs kPrefetchTiles tiles ahead of the TMA loads so that they
       // find their pages in L2 (deeper than the two shared-memory stages allow).
-      int pf_u = blockIdx.x, pf_k = (pf_u < num_units) ? p.units[pf_u].key_lo : 0;
+      int pf_u = blockIdx.x;
+      UnitInfo pu = (pf_u < num_units) ? get_unit(args, num_units, pf_u) : UnitInfo{};
+      int pf_k = pu.key_lo;
       uint32_t pf_tiles = 0;
       auto prefetch_upto = [&](uint32_t target) {
         while (pf_tiles < target && pf_u < num_units) {
-          const Unit pu = p.units[pf_u];
+          if (pf_k >= pu.key_hi) {  // empty unit
+            pf_u += gridDim.x;
+            if (pf_u < num_units) pu = get_unit(args, num_units, pf_u);
+            pf_k = pu.key_lo;
+            continue;
+          }
           for (int h = 0; h < 2; ++h) {
             const int kk = pf_k + 64 * h;
             if (kk < pu.key_hi) {
@@ -257,14 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++pf_tiles;
           pf_k += kTileKeys;
-          if (pf_k >= pu.key_hi) {
-            pf_u += gridDim.x;
-            if (pf_u < num_units) pf_k = p.units[pf_u].key_lo;
-          }
         }
       };
       for (int u = blockIdx.x; u < num_units && !aborted(ms); u += gridDim.x) {
-        const Unit un = p.units[u];
+        const UnitInfo un = get_unit(args, num_units, u);
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
           const int s = fill % kStages;
           const uint32_t n = fill / kStages;
@@ -306,16 +352,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, 128, C::NQK);
       constexpr uint32_t idesc_pv = instr_desc(0, 0, 1, 1, 128, C::NPV);
       const uint32_t q_s0 = smem_addr(qbuf), p_s = smem_addr(pbuf);
-      auto tiles_of = [&](int u) {
-        const Unit un = p.units[u];
-        return (un.key_hi - un.key_lo + kTileKeys - 1) / kTileKeys;
+      auto tiles_of = [&](int u) { return tiles_in(get_unit(args, num_units, u)); };
+      // next unit (from u on, stepping by the grid) that has at least one key tile
+      auto next_busy = [&](int u, int* n) {
+        while (u < num_units && (*n = tiles_of(u)) == 0) u += gridDim.x;
+        return u;
       };
       // scores cursor
-      int qu = blockIdx.x, qt = 0, qn = (qu < num_units) ? tiles_of(qu) : 0;
+      int qn = 0, qt = 0;
+      int qu = next_busy(blockIdx.x, &qn);
       uint32_t qg = 0, q_units = 0;
       bool q_ready = false;
       // values cursor
-      int pu = blockIdx.x, pt = 0, pn = qn;
+      int pu = qu, pt = 0, pn = qn;
       uint32_t pg = 0;
       uint64_t idle_since = globaltimer_ns();
       while (pu < num_units) {
@@ -350,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++pt == pn) {
             pu += gridDim.x;
             pt = 0;
-            pn = (pu < num_units) ? tiles_of(pu) : 0;
+            pu = next_busy(pu, &pn);
           }
           progress = true;
         }
@@ -391,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               qt = 0;
               q_ready = false;
               ++q_units;
-              qn = (qu < num_units) ? tiles_of(qu) : 0;
+              qu = next_busy(qu, &qn);
             }
             progress = true;
           }
@@ -413,15 +462,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // power-of-two scale, as soon as the previous unit's scores stopped reading it; the
     // softmax warps meanwhile finish the previous unit.
     const int w2 = warp - 2;
-    const int R = args.rows;
     const float kv_scale = p.kv_scale;
-    uint32_t k = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++k) {
+    uint32_t k = 0;  // units with work, in order
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const UnitInfo ui = get_unit(args, num_units, u);
+      if (tiles_in(ui) == 0) continue;
+      const int R = ui.rows;
       const int slot = k % C::kQB;
       if (k >= (uint32_t)C::kQB && !wait_or_abort(&ms->q_empty[slot], ((k / C::kQB) - 1) & 1, ms, p)) break;
       uint8_t* qdst = qbuf + slot * C::kQBytes;
       float* row_scale = ms->row_scale[k & 1];
-      const uint16_t* qseq = p.q + (int64_t)p.units[u].b * p.R * kD;
+      const uint16_t* qseq = p.q + (int64_t)ui.qrow0 * kD;
       // rows r0, r0+2, r0+4, r0+6 of this warp: all loads first, then the arithmetic
       for (int r0 = w2; r0 < RP; r0 += 8) {
         uint4 ld[4][2], tl[4][2];
@@ -499,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&ms->q_full[slot]);
+      ++k;
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------------ softmax warpgroups
@@ -510,9 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;  // TMEM lane quadrant
     const int i = wq * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-    const int R = args.rows;
     const float kv_scale = p.kv_scale;
-    uint32_t tile = 0, pv_waits = 0, wg_phase = 0, k = 0;
+    uint32_t tile = 0, pv_waits = 0, wg_phase = 0, k = 0;  // k: units with work, in order
     uint64_t* wg_bar = &ms->wg_bar[wg];
     // Bounded warpgroup barrier: every thread arrives, then waits for the phase.
     auto wg_sync = [&]() -> bool {
@@ -522,23 +573,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       return good;
     };
     bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++k) {
-      const Unit un = p.units[u];
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const UnitInfo un = get_unit(args, num_units, u);
+      const int R = un.rows;
+      const int ntiles = tiles_in(un);
+      const bool final_out = un.final_out != 0;
+      if (ntiles == 0) {  // no visible key at all: out = 0, lse = -inf
+        for (int r = rb; r < rb + RH && r < R; ++r) {
+          const int64_t row = (int64_t)un.qrow0 + ms->row_off[r];
+          for (int dv = i; dv < kDV; dv += 128) p.out[row * kDV + dv] = 0;
+          if (i == 0 && p.lse) p.lse[row] = -INFINITY;
+        }
+        continue;
+      }
       const int L = seq_len_of(p, un.b);
-      const int ntiles = (un.key_hi - un.key_lo + kTileKeys - 1) / kTileKeys;
-      const bool final_out = p.seqs[un.b].count == 1;
       if (wg == 0) {  // warm L2 with the next unit's query rows (9 lines of 128 bytes per row)
         const int un_next = u + gridDim.x;
         if (un_next < num_units) {
-          const int bn = p.units[un_next].b;
-          if (bn != un.b)
-            for (int x = i; x < R * 9; x += 128)
-              prefetch_l2(reinterpret_cast<const uint8_t*>(p.q + ((int64_t)bn * p.R + ms->row_off[x / 9]) * kD) + (x % 9) * 128);
+          const UnitInfo nx = get_unit(args, num_units, un_next);
+          if (nx.qrow0 != un.qrow0)
+            for (int x = i; x < nx.rows * 9; x += 128)
+              prefetch_l2(reinterpret_cast<const uint8_t*>(p.q + ((int64_t)nx.qrow0 + ms->row_off[x / 9]) * kD) + (x % 9) * 128);
         }
       }
       // last visible key of new position j is L - n_q + j (and the unit ends at key_hi)
       const int lim_cap = un.key_hi - 1;
-      const int lim0 = min(lim_cap, L - p.n_q);
+      const int lim0 = min(lim_cap, L - p.n_q + un.j0);
       // this unit's row scales (staged with its query terms)
       if (!(ok = wait_or_abort(&ms->q_full[k % C::kQB], (k / C::kQB) & 1, ms, p))) break;
       float rs[RH], m[RH], l[RH];
@@ -722,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int dv = c * 128 + i;
           const int roff = ms->row_off[rb + r];
           if (final_out) {
-            p.out[((int64_t)un.b * p.R + roff) * kDV + dv] =
+            p.out[((int64_t)un.qrow0 + roff) * kDV + dv] =
                 __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv[r]));
           } else {
             p.part_out[((int64_t)u * p.R + roff) * kDV + dv] = acc * inv[r];
@@ -741,11 +801,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse = (lt > 0.f) ? 0.6931471805599453f * (mm - kPScale + log2f(lt)) : -INFINITY;
         const int roff = ms->row_off[rb + i];
         if (final_out) {
-          if (p.lse) p.lse[(int64_t)un.b * p.R + roff] = lse;
+          if (p.lse) p.lse[(int64_t)un.qrow0 + roff] = lse;
         } else {
           p.part_lse[(int64_t)u * p.R + roff] = lse;
         }
       }
+      ++k;
     }
   }
 
@@ -841,7 +902,9 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
     a.h0 = gi * a.Hs;
     if (gi == groups - 1) a.Hs = p.H - a.h0;
     a.rows = p.n_q * a.Hs;
-    a.total_rows_alloc = p.R;
+    a.prefill = 0;
+    a.P = 0;
+    a.num_units = 0;
     cudaError_t e;
     if (a.rows <= 16)
       e = launch_rp<16>(a, mm, mt, grid, s);
@@ -853,6 +916,26 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
     ++*launches;
   }
   return cudaSuccess;
+}
+
+// Causal prefill of one sequence: units are blocks of P = 48 / H new positions (all their
+// heads, at most 48 rows) over every key they see, handed out longest first. No split of
+// the key axis (there are thousands of units), so no planner and no merge.
+cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches) {
+  CUtensorMap mm, mt;
+  if (!encode_pool_maps(p, &mm, &mt)) return cudaErrorInvalidValue;
+  DecodeArgs a;
+  a.p = p;
+  a.h0 = 0;
+  a.Hs = p.H;
+  a.P = 48 / p.H;
+  a.rows = a.P * p.H;
+  a.prefill = 1;
+  a.num_units = (p.n_q + a.P - 1) / a.P;
+  const int grid = min(num_sms, a.num_units);
+  const cudaError_t e = launch_rp<48>(a, mm, mt, grid, s);
+  if (e == cudaSuccess) ++*launches;
+  return e;
 }
 
 }  // namespace mla

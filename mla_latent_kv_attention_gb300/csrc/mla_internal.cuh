@@ -87,8 +87,8 @@ __device__ __forceinline__ void report(WsHeader* hdr, mla_status_t code) {
 // Launchers (each returns the CUDA error of its launch).
 cudaError_t launch_plan(const AttnParams& p, int target_units, cudaStream_t s);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s);
-cudaError_t launch_attn_v0(const AttnParams& p, bool prefill, int T, cudaStream_t s);
 cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
+cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
                                     uint16_t* out, float* lse, cudaStream_t s);
 cudaError_t launch_reset_status(WsHeader* hdr, cudaStream_t s);
