@@ -131,7 +131,7 @@ class ClockSampler:
 def kernel_traffic(kernel_file):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if the
     summary was taken on the current source of that kernel; else None."""
-    summary = os.path.join(ROOT, "profiles", "decode_split_kernel_batched_paged_decode.md")
+    summary = os.path.join(ROOT, "profiles", "attn_tc_kernel_batched_paged_decode.md")
     src = os.path.join(ROOT, "mla_latent_kv_attention_gb300", "csrc", kernel_file)
     if not (os.path.exists(summary) and os.path.exists(src)):
         return None
@@ -283,8 +283,10 @@ def bench_ours(args, world, rank, local):
 
     line = None
     if rank == 0:
+        _, bf16_peak, _ = load_peaks()
+        secondary = secondary_workloads(dev, hbm_peak, bf16_peak, args.steps) if args.all else None
         achieved = nbytes / (kms / 1e3) / 1e9
-        traffic = kernel_traffic("mla_decode_tc.cu")
+        traffic = kernel_traffic("mla_attention_tc.cu")
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -299,14 +301,81 @@ def bench_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": traffic,
-                         "kernel": "split-KV attention kernel (CUDA events around its launch)",
+                         "kernel": "attn_tc_kernel (split-KV attention; CUDA events around its launch)",
                          "kernel_ms": kms, "peak_source": f"{peak_src} hbm_gbs"},
             "e2e": {"value": world * nbytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
+        if secondary is not None:
+            line["other_workloads"] = secondary
     return line
+
+
+def _time_events(fn, steps, warmup):
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
+    """The other named workloads, timed the same way (inputs rotated past L2 where they
+    would fit in it); reported next to the headline, not as bench lines of their own."""
+    import torch
+
+    import mla_latent_kv_attention_gb300 as mla
+    from mla_latent_kv_attention_gb300 import accounting, workloads as W
+
+    res = {}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    decode_cases = [(f"long_history_h{H}", W.long_history_decode(H)) for H in (8, 12, 16)]
+    decode_cases.append(("spec_verify", W.spec_verify()))
+    for name, inp in decode_cases:
+        copies = max(2, math.ceil(3 * l2 / inp.pool.numel()))
+        sets = []
+        for _ in range(copies):
+            kv = mla.KVCache.from_inputs(inp, dev)
+            q = inp.q.contiguous().to(dev)
+            ws = mla.workspace(mla.MLA_OP_VERIFY, inp.B, inp.H, inp.n_q, dev)
+            out = torch.empty(inp.B, inp.n_q, inp.H, 512, dtype=torch.bfloat16, device=dev)
+            lse = torch.empty(inp.B, inp.n_q, inp.H, dtype=torch.float32, device=dev)
+            sets.append((kv, q, ws, out, lse))
+
+        def run(i, sets=sets, inp=inp):
+            kv, q, ws, out, lse = sets[i % len(sets)]
+            mla.mla_verify(kv, q, inp.sm_scale, out=out, lse=lse, ws=ws)
+
+        ms = _time_events(run, steps, 3)
+        nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), inp.n_q, inp.H)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"us_per_layer": ms * 1e3, "GB_s": gbs, "frac_of_hbm_peak": gbs / hbm_peak,
+                     "launches_per_call": mla.mla_last_launch_count(),
+                     "algorithmic_bytes": nbytes, "B": inp.B, "H": inp.H, "n_q": inp.n_q}
+        del sets
+    inp = W.causal_prefill()
+    kv = mla.KVCache.from_inputs(inp, dev)
+    q = inp.q[0].contiguous().to(dev)
+    ws = mla.workspace(mla.MLA_OP_PREFILL, 1, inp.H, inp.n_q, dev)
+    out = torch.empty(inp.n_q, inp.H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(inp.n_q, inp.H, dtype=torch.float32, device=dev)
+    ms = _time_events(lambda i: mla.mla_prefill(kv, q, inp.sm_scale, out=out, lse=lse, ws=ws),
+                      max(3, steps // 5), 2)
+    flops = accounting.attention_flops(inp.seq_lens.tolist(), inp.n_q, inp.H)
+    tf = flops / (ms / 1e3) / 1e12
+    res["causal_prefill"] = {"ms_per_chunk": ms, "tok_s": inp.n_q / (ms / 1e3), "TFLOP_s": tf,
+                             "frac_of_bf16_peak": tf / bf16_peak,
+                             "algorithmic_flops": flops, "T": inp.n_q, "prefix": 32768, "H": inp.H}
+    return res
 
 
 def cpu_baseline(line):
@@ -335,6 +404,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", dest="all", action="store_false",
+                    help="skip the secondary workloads (long history, verify, prefill)")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

@@ -1,4 +1,5 @@
-// mla_decode_tc.cu -- split-KV decode / speculative-verify attention on tcgen05 tensor cores.
+// mla_attention_tc.cu -- MLA attention on tcgen05 tensor cores: split-KV decode, speculative
+// verify and causal prefill over the paged FP8 latent cache.
 //
 // Work: one persistent CTA per SM walks the planner's units (keys [key_lo, key_hi) of one
 // sequence, all of its query rows). Keys stream through shared memory 128 at a time
@@ -225,7 +226,7 @@ __device__ __forceinline__ int q_offset(int n, int w16) {
 
 template <int RP>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ DecodeArgs args,
+    attn_tc_kernel(const __grid_constant__ DecodeArgs args,
                      const __grid_constant__ CUtensorMap map_main,
                      const __grid_constant__ CUtensorMap map_tail) {
   using C = Cfg<RP>;
@@ -870,7 +871,7 @@ template <int RP>
 cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensorMap& mt,
                       int grid, cudaStream_t s) {
   constexpr int smem = smem_bytes<RP>();
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<RP>,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<RP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -883,7 +884,7 @@ cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensor
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<RP>, a, mm, mt);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<RP>, a, mm, mt);
 }
 
 }  // namespace
