@@ -89,9 +89,12 @@ mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
   p.seqs = reinterpret_cast<mla::SeqUnits*>(base + w.seqs);
   p.part_lse = reinterpret_cast<float*>(base + w.part_lse);
   p.part_out = reinterpret_cast<float*>(base + w.part_out);
+  p.cta_first = reinterpret_cast<int*>(base + w.cta_first);
+  p.blk_prefix = reinterpret_cast<int*>(base + w.blk_prefix);
   p.max_units = w.max_units;
+  p.num_ctas = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mla::launch_plan(p, mla::kUnitsPerSm * sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (mla::launch_plan(p, s) != cudaSuccess) return MLA_ERR_CUDA;
   ++g_last_launches;
   prof_mark(g_prof_start, s);
   int launched = 0;

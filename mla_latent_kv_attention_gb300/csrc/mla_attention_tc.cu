@@ -274,6 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int num_units = args.prefill ? args.num_units : p.hdr->num_units;
+  // this CTA's units: a contiguous range from the planner (decode/verify), or every
+  // gridDim.x-th unit (prefill)
+  const int u_begin = args.prefill ? (int)blockIdx.x : p.cta_first[blockIdx.x];
+  const int u_end = args.prefill ? num_units : p.cta_first[blockIdx.x + 1];
+  const int u_step = args.prefill ? (int)gridDim.x : 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -283,15 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fill = 0;  // tiles issued so far
       // L2 prefetch cursor: runs kPrefetchTiles tiles ahead of the TMA loads so that they
       // find their pages in L2 (deeper than the two shared-memory stages allow).
-      int pf_u = blockIdx.x;
-      UnitInfo pu = (pf_u < num_units) ? get_unit(args, num_units, pf_u) : UnitInfo{};
+      int pf_u = u_begin;
+      UnitInfo pu = (pf_u < u_end) ? get_unit(args, num_units, pf_u) : UnitInfo{};
       int pf_k = pu.key_lo;
       uint32_t pf_tiles = 0;
       auto prefetch_upto = [&](uint32_t target) {
-        while (pf_tiles < target && pf_u < num_units) {
-          if (pf_k >= pu.key_hi) {  // empty unit
-            pf_u += gridDim.x;
-            if (pf_u < num_units) pu = get_unit(args, num_units, pf_u);
+        while (pf_tiles < target && pf_u < u_end) {
+          if (pf_k >= pu.key_hi) {  // unit done (or empty)
+            pf_u += u_step;
+            if (pf_u < u_end) pu = get_unit(args, num_units, pf_u);
             pf_k = pu.key_lo;
             continue;
           }
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf_k += kTileKeys;
         }
       };
-      for (int u = blockIdx.x; u < num_units && !aborted(ms); u += gridDim.x) {
+      for (int u = u_begin; u < u_end && !aborted(ms); u += u_step) {
         const UnitInfo un = get_unit(args, num_units, u);
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
           const int s = fill % kStages;
@@ -356,19 +361,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto tiles_of = [&](int u) { return tiles_in(get_unit(args, num_units, u)); };
       // next unit (from u on, stepping by the grid) that has at least one key tile
       auto next_busy = [&](int u, int* n) {
-        while (u < num_units && (*n = tiles_of(u)) == 0) u += gridDim.x;
+        while (u < u_end && (*n = tiles_of(u)) == 0) u += u_step;
         return u;
       };
       // scores cursor
       int qn = 0, qt = 0;
-      int qu = next_busy(blockIdx.x, &qn);
+      int qu = next_busy(u_begin, &qn);
       uint32_t qg = 0, q_units = 0;
       bool q_ready = false;
       // values cursor
       int pu = qu, pt = 0, pn = qn;
       uint32_t pg = 0;
       uint64_t idle_since = globaltimer_ns();
-      while (pu < num_units) {
+      while (pu < u_end) {
         bool progress = false;
         // values first: a finished PV hands its KV stage back to the producer
         if (pg < qg && mbar_test_wait(&ms->p_full, pg & 1)) {
@@ -398,13 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&ms->pv_done);
           ++pg;
           if (++pt == pn) {
-            pu += gridDim.x;
+            pu += u_step;
             pt = 0;
             pu = next_busy(pu, &pn);
           }
           progress = true;
         }
-        if (qu < num_units) {
+        if (qu < u_end) {
           const int s = qg % kStages, sb = qg & 1;
           bool ready = true;
           const int qslot = q_units % C::kQB;
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++qg;
             if (++qt == qn) {
               mma_commit(&ms->q_empty[qslot]);  // that query buffer is free once these complete
-              qu += gridDim.x;
+              qu += u_step;
               qt = 0;
               q_ready = false;
               ++q_units;
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w2 = warp - 2;
     const float kv_scale = p.kv_scale;
     uint32_t k = 0;  // units with work, in order
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    for (int u = u_begin; u < u_end; u += u_step) {
       const UnitInfo ui = get_unit(args, num_units, u);
       if (tiles_in(ui) == 0) continue;
       const int R = ui.rows;
@@ -574,23 +579,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       return good;
     };
     bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+    for (int u = u_begin; u < u_end && ok; u += u_step) {
       const UnitInfo un = get_unit(args, num_units, u);
       const int R = un.rows;
       const int ntiles = tiles_in(un);
       const bool final_out = un.final_out != 0;
-      if (ntiles == 0) {  // no visible key at all: out = 0, lse = -inf
+      if (ntiles == 0) {  // no visible key at all: out = 0, lse = -inf (or an empty partial)
         for (int r = rb; r < rb + RH && r < R; ++r) {
-          const int64_t row = (int64_t)un.qrow0 + ms->row_off[r];
-          for (int dv = i; dv < kDV; dv += 128) p.out[row * kDV + dv] = 0;
-          if (i == 0 && p.lse) p.lse[row] = -INFINITY;
+          if (final_out) {
+            const int64_t row = (int64_t)un.qrow0 + ms->row_off[r];
+            for (int dv = i; dv < kDV; dv += 128) p.out[row * kDV + dv] = 0;
+            if (i == 0 && p.lse) p.lse[row] = -INFINITY;
+          } else if (i == 0) {
+            p.part_lse[(int64_t)u * p.R + ms->row_off[r]] = -INFINITY;
+          }
         }
         continue;
       }
       const int L = seq_len_of(p, un.b);
       if (wg == 0) {  // warm L2 with the next unit's query rows (9 lines of 128 bytes per row)
-        const int un_next = u + gridDim.x;
-        if (un_next < num_units) {
+        const int un_next = u + u_step;
+        if (un_next < u_end) {
           const UnitInfo nx = get_unit(args, num_units, un_next);
           if (nx.qrow0 != un.qrow0)
             for (int x = i; x < nx.rows * 9; x += 128)
@@ -894,7 +903,8 @@ cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensor
 cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches) {
   CUtensorMap mm, mt;
   if (!encode_pool_maps(p, &mm, &mt)) return cudaErrorInvalidValue;
-  const int grid = min(num_sms, p.max_units);
+  const int grid = p.num_ctas;  // the planner cut the work into this many ranges
+  (void)num_sms;
   const int groups = (p.R > 48) ? 2 : 1;
   for (int gi = 0; gi < groups; ++gi) {
     DecodeArgs a;

@@ -11,7 +11,6 @@ namespace mla {
 constexpr int kD = MLA_D;
 constexpr int kDV = MLA_DV;
 constexpr int kKeyBlock = 128;     // keys per work block: the unit of split planning
-constexpr int kUnitsPerSm = 2;     // split-KV target: about this many units per SM
 constexpr int kMaxRows = MLA_MAX_HEADS * MLA_MAX_NQ;  // query rows per sequence (64)
 
 // Workspace header at offset 0 (256 bytes).
@@ -34,15 +33,18 @@ struct SeqUnits {
 
 // Offsets of the workspace regions for one decode/verify call.
 struct WsLayout {
-  size_t hdr, units, seqs, part_lse, part_out, total;
-  int max_units;
+  size_t hdr, units, seqs, cta_first, blk_prefix, part_lse, part_out, total;
+  int max_units, max_ctas;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline WsLayout ws_layout(int B, int rows_per_seq, int num_sms) {
   WsLayout w;
-  w.max_units = kUnitsPerSm * num_sms + B;
+  // one contiguous block range per CTA, split only where a sequence ends: at most
+  // (CTAs + B - 1) pieces
+  w.max_ctas = num_sms;
+  w.max_units = num_sms + B;
   size_t off = 0;
   w.hdr = off;
   off += sizeof(WsHeader);
@@ -50,6 +52,10 @@ inline WsLayout ws_layout(int B, int rows_per_seq, int num_sms) {
   off += sizeof(Unit) * (size_t)w.max_units;
   w.seqs = off = align_up(off, 256);
   off += sizeof(SeqUnits) * (size_t)(B > 0 ? B : 1);
+  w.cta_first = off = align_up(off, 256);
+  off += sizeof(int) * (size_t)(num_sms + 1);
+  w.blk_prefix = off = align_up(off, 256);
+  off += sizeof(int) * (size_t)(B + 1);
   w.part_lse = off = align_up(off, 256);
   off += sizeof(float) * (size_t)w.max_units * rows_per_seq;
   w.part_out = off = align_up(off, 256);
@@ -76,8 +82,11 @@ struct AttnParams {
   float* part_lse;    // [max_units][R]
   Unit* units;
   SeqUnits* seqs;
+  int* cta_first;   // [num_ctas + 1]: CTA c owns units [cta_first[c], cta_first[c + 1])
+  int* blk_prefix;  // [B + 1]: first 128-key block of each sequence in the flat block order
   WsHeader* hdr;
   int max_units;
+  int num_ctas;
 };
 
 __device__ __forceinline__ void report(WsHeader* hdr, mla_status_t code) {
@@ -85,7 +94,7 @@ __device__ __forceinline__ void report(WsHeader* hdr, mla_status_t code) {
 }
 
 // Launchers (each returns the CUDA error of its launch).
-cudaError_t launch_plan(const AttnParams& p, int target_units, cudaStream_t s);
+cudaError_t launch_plan(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);

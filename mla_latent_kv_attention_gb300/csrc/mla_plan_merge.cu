@@ -1,7 +1,7 @@
 // mla_plan_merge.cu -- split-KV planning and the log-sum-exp merge.
 //
-// Planning: the key axis of every sequence is cut into units of whole 128-key blocks so
-// that the number of units is about kUnitsPerSm x SMs and units are balanced in keys.
+// Planning: the key axis of every sequence is cut into units of whole 128-key blocks; the
+// blocks of all sequences are shared out evenly, one contiguous range per CTA.
 // A long history therefore spreads over all SMs, which is what made the pages' decode
 // faster ("Scaling Kimi K3 on AMD Instinct MI355X", section "并行度必须适配真正的形状":
 // the long history handed to more work groups), while short batches stay one unit per
@@ -20,6 +20,13 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+
+// Cached length clamped to what the page table can hold (no status report).
+__device__ int clamp_len_quiet(const AttnParams& p, int b) {
+  const int L = p.seq_lens[b];
+  const int64_t cap = p.pt_stride * (int64_t)p.page_size;
+  return L < 0 ? 0 : ((int64_t)L > cap ? (int)cap : L);
+}
 
 __device__ int clamp_len(const AttnParams& p, int b) {
   int L = p.seq_lens[b];
@@ -69,8 +76,21 @@ __device__ int block_scan(int v, int* scratch, int* total) {
   return x + prefix;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p, int target_units) {
-  __shared__ long long s_ll[32];
+// First block of CTA c's range when `total` blocks are cut into n nearly equal ranges.
+__device__ __forceinline__ int64_t range_lo(int64_t c, int64_t total, int64_t n) {
+  return c * total / n;
+}
+// The CTA whose range holds block x: the largest c with range_lo(c) <= x.
+__device__ __forceinline__ int64_t range_of(int64_t x, int64_t total, int64_t n) {
+  return ((x + 1) * n + total - 1) / total - 1;
+}
+
+// Split planning: the 128-key blocks of all sequences, laid end to end, are cut into one
+// contiguous range per CTA of nearly equal size; a CTA's range becomes one unit per
+// sequence it touches. Every CTA gets the same amount of key traffic, a sequence is split
+// only where a range boundary falls inside it, and units are numbered in block order, so
+// each sequence's units and each CTA's units are contiguous.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p) {
   __shared__ int s_i[32];
   // the attention kernel may start its prologue now; it waits for this grid before
   // reading the plan
@@ -86,102 +106,150 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p, int ta
   }
   if (tid == 0) p.hdr->status = 0;  // this call's status word starts clean
   __syncthreads();
-  long long blocks = 0;
-  for (int b = tid; b < p.B; b += blockDim.x) {
-    int L = clamp_len(p, b);
-    blocks += (L + kKeyBlock - 1) / kKeyBlock;
-  }
-  long long total = block_reduce(blocks, [](long long a, long long c) { return a + c; }, s_ll);
-  int bpu = (int)((total + target_units - 1) / target_units);
-  if (bpu < 1) bpu = 1;
+  // 1. blocks per sequence -> exclusive prefix in flat block order
   int carry = 0;
   for (int base = 0; base < p.B; base += blockDim.x) {
     const int b = base + tid;
-    int L = 0, n = 0;
-    if (b < p.B) {
-      L = clamp_len(p, b);
-      int nb = (L + kKeyBlock - 1) / kKeyBlock;
-      n = (nb + bpu - 1) / bpu;
-    }
+    const int nb = (b < p.B) ? (clamp_len(p, b) + kKeyBlock - 1) / kKeyBlock : 0;
     int chunk_total;
-    int incl = block_scan(n, s_i, &chunk_total);
-    int first = carry + incl - n;
-    if (b < p.B) {
-      p.seqs[b] = SeqUnits{first, n};
-      for (int k = 0; k < n; ++k) {
-        int lo = k * bpu * kKeyBlock;
-        int hi = min(L, (k + 1) * bpu * kKeyBlock);
-        p.units[first + k] = Unit{b, lo, hi, first + k};
-      }
-    }
+    const int incl = block_scan(nb, s_i, &chunk_total);
+    if (b < p.B) p.blk_prefix[b] = carry + incl - nb;
     carry += chunk_total;
     __syncthreads();
   }
+  const int64_t total = carry;
+  const int64_t n = p.num_ctas;
+  if (tid == 0) p.blk_prefix[p.B] = carry;
+  __syncthreads();
+  // 2. pieces per sequence (one per CTA range it overlaps): counts and first unit index
+  int ucarry = 0;
+  for (int base = 0; base < p.B; base += blockDim.x) {
+    const int b = base + tid;
+    int cnt = 0;
+    if (b < p.B) {
+      const int start = p.blk_prefix[b], nb = p.blk_prefix[b + 1] - start;
+      // with at least one block per CTA every range is non-empty; with fewer blocks than
+      // CTAs each block is a range of its own
+      if (nb > 0)
+        cnt = (total >= n) ? (int)(range_of(start + nb - 1, total, n) - range_of(start, total, n) + 1)
+                           : nb;
+    }
+    int chunk_total;
+    const int incl = block_scan(cnt, s_i, &chunk_total);
+    if (b < p.B) p.seqs[b] = SeqUnits{ucarry + incl - cnt, cnt};
+    ucarry += chunk_total;
+    __syncthreads();
+  }
+  const int num_units = ucarry;
+  // 3. per CTA range (one thread each): its first unit, and the units it owns: one per
+  //    sequence the range touches, numbered in block order
+  for (int c = tid; c <= p.num_ctas; c += blockDim.x) {
+    const int64_t x0 = range_lo(c, total, n);
+    const int64_t x1 = (c < p.num_ctas) ? range_lo(c + 1, total, n) : x0;
+    int first = num_units;
+    if (x0 < total) {
+      int lo = 0, hi = p.B - 1;  // last sequence b with blk_prefix[b] <= x0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (p.blk_prefix[mid] <= x0) lo = mid; else hi = mid - 1;
+      }
+      // the unit holding block x0 (sequence lo holds it); an empty range owns nothing and
+      // points at the next range's first unit
+      const int start_lo = p.blk_prefix[lo];
+      first = p.seqs[lo].first + ((total >= n)
+                                      ? (int)(range_of(x0, total, n) - range_of(start_lo, total, n))
+                                      : (int)(x0 - start_lo));
+      for (int b = lo; b < p.B && p.blk_prefix[b] < x1; ++b) {
+        const int start = p.blk_prefix[b], end = p.blk_prefix[b + 1];
+        if (end <= x0 || end == start) continue;
+        const int64_t plo = max((int64_t)start, x0), phi = min((int64_t)end, x1);
+        const int k = (total >= n) ? (int)(range_of(plo, total, n) - range_of(start, total, n))
+                                   : (int)(plo - start);
+        const int idx = p.seqs[b].first + k;
+        if (phi <= plo) continue;  // an empty range owns nothing
+        const int L = clamp_len_quiet(p, b);
+        p.units[idx] = Unit{b, (int)(plo - start) * kKeyBlock,
+                            min(L, (int)(phi - start) * kKeyBlock), idx};
+      }
+    }
+    p.cta_first[c] = first;
+  }
   if (tid == 0) {
-    p.hdr->num_units = carry;
-    p.hdr->blocks_per_unit = bpu;
+    p.hdr->num_units = num_units;
+    p.hdr->blocks_per_unit = (int)((total + n - 1) / n);
   }
 }
 
-constexpr int kMergeWarps = 4;
+constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = 32 * kMergeWarps;
-constexpr int kMergeChunks = kDV / 128;  // one CTA per (row, 128-wide dv chunk)
+constexpr int kMergeMaxCached = 1024;  // partial weights kept in shared memory per row
 
-// Merge one 128-wide dv chunk of one row. Partial u of the row sits at
-// po + (base + u * stride) * 512 and pl[base + u * stride]. Every thread scans all the
-// lse values itself (they are few and cached); warp w sums partials w, w + 4, ...;
-// lane l owns four consecutive outputs.
+// Merge one dv chunk (W = 4 * 32 or 1 * 32 values) of one row. Partial u of the row sits
+// at po + (base + u * stride) * 512 and pl[base + u * stride]. The block reduces the lse
+// values together (max, then sum of exponentials) and keeps the weights in shared memory;
+// warp w then sums partials w, w + 8, ... with lane l owning VEC consecutive outputs.
+template <int VEC>
 __device__ void merge_chunk(const float* __restrict__ po, const float* __restrict__ pl,
                             int64_t base, int64_t stride, int count, int chunk,
                             uint16_t* __restrict__ out_row, float* lse_out) {
-  __shared__ float4 s_acc[kMergeWarps][32];
+  constexpr int W = 32 * VEC;  // dv per CTA
+  __shared__ float s_red[32];
+  __shared__ float s_w[kMergeMaxCached];
+  __shared__ float s_acc[kMergeWarps][W];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float m = -INFINITY;
-#pragma unroll 8
-  for (int u = 0; u < count; ++u) m = fmaxf(m, pl[base + (int64_t)u * stride]);
+  for (int u = threadIdx.x; u < count; u += blockDim.x) m = fmaxf(m, pl[base + (int64_t)u * stride]);
+  m = block_reduce(m, [](float a, float c) { return fmaxf(a, c); }, s_red);
   float sum = 0.f;
-  if (m != -INFINITY) {
-#pragma unroll 8
-    for (int u = 0; u < count; ++u) sum += expf(pl[base + (int64_t)u * stride] - m);
-  }
+  if (m != -INFINITY)
+    for (int u = threadIdx.x; u < count; u += blockDim.x) sum += expf(pl[base + (int64_t)u * stride] - m);
+  sum = block_reduce(sum, [](float a, float c) { return a + c; }, s_red);
   const float lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (m != -INFINITY) {
+  const int cached = min(count, kMergeMaxCached);
+  for (int u = threadIdx.x; u < cached; u += blockDim.x)
+    s_w[u] = (m == -INFINITY) ? 0.f : expf(pl[base + (int64_t)u * stride] - lse);
+  __syncthreads();
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
 #pragma unroll 4
-    for (int u = warp; u < count; u += kMergeWarps) {
-      const int64_t r = base + (int64_t)u * stride;
-      const float w = expf(pl[r] - lse);
-      if (w == 0.f) continue;  // an empty partial (lse = -inf) holds no data worth reading
-      const float4 v = reinterpret_cast<const float4*>(po + r * kDV + chunk * 128)[lane];
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+  for (int u = warp; u < count; u += kMergeWarps) {
+    const int64_t r = base + (int64_t)u * stride;
+    const float w = (u < kMergeMaxCached) ? s_w[u]
+                                          : ((m == -INFINITY) ? 0.f : expf(pl[r] - lse));
+    if (w == 0.f) continue;  // an empty partial (lse = -inf) holds no data worth reading
+    const float* src = po + r * kDV + chunk * W + lane * VEC;
+    if (VEC == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x;
+      acc[VEC > 1 ? 1 : 0] += w * v.y;
+      acc[VEC > 2 ? 2 : 0] += w * v.z;
+      acc[VEC > 3 ? 3 : 0] += w * v.w;
+    } else {
+      acc[0] += w * src[0];
     }
   }
-  s_acc[warp][lane] = acc;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) s_acc[warp][lane * VEC + e] = acc[e];
   __syncthreads();
   if (warp == 0) {
-    float4 t = s_acc[0][lane];
+    float t[VEC];
 #pragma unroll
-    for (int g = 1; g < kMergeWarps; ++g) {
-      t.x += s_acc[g][lane].x;
-      t.y += s_acc[g][lane].y;
-      t.z += s_acc[g][lane].z;
-      t.w += s_acc[g][lane].w;
+    for (int e = 0; e < VEC; ++e) {
+      t[e] = 0.f;
+#pragma unroll
+      for (int g = 0; g < kMergeWarps; ++g) t[e] += s_acc[g][lane * VEC + e];
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
-    uint2 packed;
-    packed.x = *reinterpret_cast<unsigned int*>(&lo);
-    packed.y = *reinterpret_cast<unsigned int*>(&hi);
-    reinterpret_cast<uint2*>(out_row + chunk * 128)[lane] = packed;
+    uint16_t* dst = out_row + chunk * W + lane * VEC;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) dst[e] = __bfloat16_as_ushort(__float2bfloat16_rn(t[e]));
   }
   if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = lse;
 }
 
 // Rows of the decode/verify path whose sequence has more (or fewer) than one unit.
 // Launched as a programmatic dependent of the attention kernel: it waits for that grid.
+template <int VEC>
 __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = blockIdx.x;  // b * R + r
@@ -189,29 +257,33 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p
   const int b = (int)(row / p.R), r = (int)(row % p.R);
   const SeqUnits su = p.seqs[b];
   if (su.count == 1) return;  // the attention kernel wrote this row directly
-  merge_chunk(p.part_out, p.part_lse, (int64_t)su.first * p.R + r, p.R, su.count, chunk,
-              p.out + row * kDV, p.lse ? p.lse + row : nullptr);
+  merge_chunk<VEC>(p.part_out, p.part_lse, (int64_t)su.first * p.R + r, p.R, su.count, chunk,
+                   p.out + row * kDV, p.lse ? p.lse + row : nullptr);
 }
 
+template <int VEC>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_standalone_kernel(const float* po, const float* pl, int S, int64_t R, uint16_t* out,
                             float* lse) {
   const int64_t row = blockIdx.x;
-  merge_chunk(po, pl, row, R, S, blockIdx.y, out + row * kDV, lse ? lse + row : nullptr);
+  merge_chunk<VEC>(po, pl, row, R, S, blockIdx.y, out + row * kDV, lse ? lse + row : nullptr);
 }
 
 __global__ void reset_status_kernel(WsHeader* hdr) { hdr->status = 0; }
 
 }  // namespace
 
-cudaError_t launch_plan(const AttnParams& p, int target_units, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p, target_units);
+cudaError_t launch_plan(const AttnParams& p, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
+  // few rows (one long sequence): narrow dv chunks so that more CTAs share the partials
+  const int rows = p.B * p.R;
+  const bool narrow = rows < 128;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * p.R), kMergeChunks);
+  cfg.gridDim = dim3((unsigned)rows, narrow ? kDV / 32 : kDV / 128);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr;
@@ -219,13 +291,17 @@ cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_split_kernel, p);
+  return narrow ? cudaLaunchKernelEx(&cfg, merge_split_kernel<1>, p)
+                : cudaLaunchKernelEx(&cfg, merge_split_kernel<4>, p);
 }
 
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
                                     uint16_t* out, float* lse, cudaStream_t s) {
-  dim3 grid((unsigned)R, kMergeChunks);
-  merge_standalone_kernel<<<grid, kMergeThreads, 0, s>>>(part_out, part_lse, S, R, out, lse);
+  if (R < 128) {
+    merge_standalone_kernel<1><<<dim3((unsigned)R, kDV / 32), kMergeThreads, 0, s>>>(part_out, part_lse, S, R, out, lse);
+  } else {
+    merge_standalone_kernel<4><<<dim3((unsigned)R, kDV / 128), kMergeThreads, 0, s>>>(part_out, part_lse, S, R, out, lse);
+  }
   return cudaGetLastError();
 }
 
