@@ -87,6 +87,7 @@ struct Misc {
   uint64_t p_full, pv_done;
   uint64_t q_full[2];   // query operand buffer holds its unit's terms
   uint64_t q_empty[2];  // the unit that used the buffer has finished its scores
+  uint64_t q0_done;     // the first unit's query rows are staged (by warps 2-11 together)
   uint64_t wg_bar[2];  // bounded barriers of the two softmax warpgroups (128 arrivals)
   uint32_t tmem_base;
   int abort;
@@ -224,6 +225,92 @@ __device__ __forceinline__ int q_offset(int n, int w16) {
   return 4 * (NQK * 128) + (n >> 3) * 512 + (n & 7) * 64 + (((w ^ ((n & 7) >> 1)) & 3) << 4);
 }
 
+// Stage rows w, w + nw, ... (< RP) of one unit's queries into a query operand buffer as two
+// e4m3 terms (a per-row power-of-two scale makes the split exact for bf16), and the rows'
+// score scales into row_scale[]. Rows at or past R are written as zeros.
+template <int RP>
+__device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int* row_off,
+                                       const uint16_t* qseq, uint8_t* qdst, float* row_scale,
+                                       int w0, int nw, int lane) {
+  using C = Cfg<RP>;
+  const float kv_scale = p.kv_scale;
+  // rows r0, r0 + nw, r0 + 2 nw, r0 + 3 nw of this warp: all loads first, then the arithmetic
+  for (int r0 = w0; r0 < RP; r0 += 4 * nw) {
+    uint4 ld[4][2], tl[4][2];
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+      const int r = r0 + nw * k2;
+      ld[k2][0] = ld[k2][1] = tl[k2][0] = tl[k2][1] = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(qseq + (int64_t)row_off[r] * kD);
+        ld[k2][0] = s4[2 * lane];
+        ld[k2][1] = s4[2 * lane + 1];
+        if (lane < 4) {  // dims 512 + 16*lane .. +15 (1024 bytes in: 64 uint4)
+          tl[k2][0] = s4[64 + 2 * lane];
+          tl[k2][1] = s4[64 + 2 * lane + 1];
+        }
+      }
+    }
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+      const int r = r0 + nw * k2;
+      if (r >= RP) break;
+      const bool real = r < R;
+      float v[16], tail[16];
+      {
+        const uint32_t w[8] = {ld[k2][0].x, ld[k2][0].y, ld[k2][0].z, ld[k2][0].w,
+                               ld[k2][1].x, ld[k2][1].y, ld[k2][1].z, ld[k2][1].w};
+        const uint32_t wt[8] = {tl[k2][0].x, tl[k2][0].y, tl[k2][0].z, tl[k2][0].w,
+                                tl[k2][1].x, tl[k2][1].y, tl[k2][1].z, tl[k2][1].w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          v[e] = __uint_as_float((w[e >> 1] >> ((e & 1) * 16)) << 16);
+          tail[e] = __uint_as_float((wt[e >> 1] >> ((e & 1) * 16)) << 16);
+        }
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fmaxf(fabsf(v[e]), fabsf(tail[e])));
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // scale 2^ex so that amax * 2^ex lies in (224, 448]; from the exponent field of
+      // amax (normal floats: biased exponent E means amax in [2^(E-127), 2^(E-126)))
+      int ex = 0;
+      if (amax >= 1.17549435e-38f && amax <= 3.4e38f) {
+        const int E = (__float_as_int(amax) >> 23) & 0xFF;
+        ex = 135 - E;  // amax * 2^ex in [256, 512)
+        if (amax * __int_as_float((127 + ex) << 23) > 448.f) ex -= 1;
+        ex = max(-126, min(126, ex));  // both 2^ex and 2^-ex stay normal floats
+      }
+      const float up = __int_as_float((127 + ex) << 23);    // 2^ex, exact
+      const float down = __int_as_float((127 - ex) << 23);  // 2^-ex, exact
+      if (lane == 0) row_scale[r] = real ? p.sm_scale * kv_scale * down * kLog2e : 0.f;
+      // two terms per value, packed 16 codes per 16-byte group
+      auto emit = [&](const float* x, int w16) {
+        uint32_t t1w[4], t2w[4];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float a0 = x[e] * up, a1 = x[e + 1] * up;
+          const uint16_t c1 = to_e4m3x2(a0, a1);
+          const float2 b1 = from_e4m3x2(c1);
+          const uint16_t c2 = to_e4m3x2(a0 - b1.x, a1 - b1.y);
+          const int wi = e >> 2, sh = (e & 2) * 8;
+          if ((e & 2) == 0) {
+            t1w[wi] = c1;
+            t2w[wi] = c2;
+          } else {
+            t1w[wi] |= (uint32_t)c1 << sh;
+            t2w[wi] |= (uint32_t)c2 << sh;
+          }
+        }
+        *reinterpret_cast<uint4*>(qdst + q_offset<C::NQK>(r, w16)) = make_uint4(t1w[0], t1w[1], t1w[2], t1w[3]);
+        *reinterpret_cast<uint4*>(qdst + q_offset<C::NQK>(RP + r, w16)) = make_uint4(t2w[0], t2w[1], t2w[2], t2w[3]);
+      };
+      emit(v, lane);
+      if (lane < 4) emit(tail, 32 + lane);
+    }
+  }
+}
+
 template <int RP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ DecodeArgs args,
@@ -255,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ms->q_full[s], 64);
       mbar_init(&ms->q_empty[s], 1);
     }
+    mbar_init(&ms->q0_done, 320);
     ms->abort = 0;
     for (int r = 0; r < 48; ++r) {
       ms->row_j[r] = (r < args.rows) ? r / args.Hs : -(1 << 30);
@@ -279,6 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int u_begin = args.prefill ? (int)blockIdx.x : p.cta_first[blockIdx.x];
   const int u_end = args.prefill ? num_units : p.cta_first[blockIdx.x + 1];
   const int u_step = args.prefill ? (int)gridDim.x : 1;
+
+  // The first unit's queries are on every CTA's critical path: warps 2-11 stage them
+  // together (about two rows each); the two stager warps then run ahead for later units.
+  if (warp >= 2) {
+    int u0 = u_begin;
+    while (u0 < u_end && tiles_in(get_unit(args, num_units, u0)) == 0) u0 += u_step;
+    if (u0 < u_end) {
+      const UnitInfo ui = get_unit(args, num_units, u0);
+      stage_rows<RP>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, qbuf,
+                     ms->row_scale[0], warp - 2, 10, lane);
+      fence_proxy_async_smem();
+      mbar_arrive(&ms->q0_done);
+    }
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -320,7 +422,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
           const int s = fill % kStages;
           const uint32_t n = fill / kStages;
-          prefetch_upto(fill + 1 + kPrefetchTiles);
           if (!wait_or_abort(&ms->kv_empty[s], (n & 1) ^ 1, ms, p)) break;
           uint8_t* st = smem + C::kOffStages + s * kStageBytes;
           mbar_arrive_expect_tx(&ms->kv_full[s], kStageBytes);
@@ -342,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + kTailOffset + h * 4096, &map_tail, 0, y, &ms->kv_full[s]);
           }
           ++fill;
+          prefetch_upto(fill + kPrefetchTiles);
         }
       }
       // Drain: wait (bounded) until the consumer released every stage still holding a load.
@@ -475,85 +577,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tiles_in(ui) == 0) continue;
       const int R = ui.rows;
       const int slot = k % C::kQB;
+      if (k == 0) {  // staged by warps 2-11 in the prologue
+        if (!wait_or_abort(&ms->q0_done, 0, ms, p)) break;
+        mbar_arrive(&ms->q_full[0]);
+        ++k;
+        continue;
+      }
       if (k >= (uint32_t)C::kQB && !wait_or_abort(&ms->q_empty[slot], ((k / C::kQB) - 1) & 1, ms, p)) break;
       uint8_t* qdst = qbuf + slot * C::kQBytes;
       float* row_scale = ms->row_scale[k & 1];
       const uint16_t* qseq = p.q + (int64_t)ui.qrow0 * kD;
-      // rows r0, r0+2, r0+4, r0+6 of this warp: all loads first, then the arithmetic
-      for (int r0 = w2; r0 < RP; r0 += 8) {
-        uint4 ld[4][2], tl[4][2];
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          const int r = r0 + 2 * k2;
-          ld[k2][0] = ld[k2][1] = tl[k2][0] = tl[k2][1] = make_uint4(0, 0, 0, 0);
-          if (r < R) {
-            const uint4* s4 = reinterpret_cast<const uint4*>(qseq + (int64_t)ms->row_off[r] * kD);
-            ld[k2][0] = s4[2 * lane];
-            ld[k2][1] = s4[2 * lane + 1];
-            if (lane < 4) {  // dims 512 + 16*lane .. +15 (1024 bytes in: 64 uint4)
-              tl[k2][0] = s4[64 + 2 * lane];
-              tl[k2][1] = s4[64 + 2 * lane + 1];
-            }
-          }
-        }
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          const int r = r0 + 2 * k2;
-          if (r >= RP) break;
-          const bool real = r < R;
-          float v[16], tail[16];
-          {
-            const uint32_t w[8] = {ld[k2][0].x, ld[k2][0].y, ld[k2][0].z, ld[k2][0].w,
-                                   ld[k2][1].x, ld[k2][1].y, ld[k2][1].z, ld[k2][1].w};
-            const uint32_t wt[8] = {tl[k2][0].x, tl[k2][0].y, tl[k2][0].z, tl[k2][0].w,
-                                    tl[k2][1].x, tl[k2][1].y, tl[k2][1].z, tl[k2][1].w};
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              v[e] = __uint_as_float((w[e >> 1] >> ((e & 1) * 16)) << 16);
-              tail[e] = __uint_as_float((wt[e >> 1] >> ((e & 1) * 16)) << 16);
-            }
-          }
-          float amax = 0.f;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fmaxf(fabsf(v[e]), fabsf(tail[e])));
-          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          // scale 2^ex so that amax * 2^ex lies in (224, 448]; from the exponent field of
-          // amax (normal floats: biased exponent E means amax in [2^(E-127), 2^(E-126)))
-          int ex = 0;
-          if (amax >= 1.17549435e-38f && amax <= 3.4e38f) {
-            const int E = (__float_as_int(amax) >> 23) & 0xFF;
-            ex = 135 - E;  // amax * 2^ex in [256, 512)
-            if (amax * __int_as_float((127 + ex) << 23) > 448.f) ex -= 1;
-            ex = max(-126, min(126, ex));  // both 2^ex and 2^-ex stay normal floats
-          }
-          const float up = __int_as_float((127 + ex) << 23);    // 2^ex, exact
-          const float down = __int_as_float((127 - ex) << 23);  // 2^-ex, exact
-          if (lane == 0) row_scale[r] = real ? p.sm_scale * kv_scale * down * kLog2e : 0.f;
-          // two terms per value, packed 16 codes per 16-byte group
-          auto emit = [&](const float* x, int w16) {
-            uint32_t t1w[4], t2w[4];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const float a0 = x[e] * up, a1 = x[e + 1] * up;
-              const uint16_t c1 = to_e4m3x2(a0, a1);
-              const float2 b1 = from_e4m3x2(c1);
-              const uint16_t c2 = to_e4m3x2(a0 - b1.x, a1 - b1.y);
-              const int wi = e >> 2, sh = (e & 2) * 8;
-              if ((e & 2) == 0) {
-                t1w[wi] = c1;
-                t2w[wi] = c2;
-              } else {
-                t1w[wi] |= (uint32_t)c1 << sh;
-                t2w[wi] |= (uint32_t)c2 << sh;
-              }
-            }
-            *reinterpret_cast<uint4*>(qdst + q_offset<C::NQK>(r, w16)) = make_uint4(t1w[0], t1w[1], t1w[2], t1w[3]);
-            *reinterpret_cast<uint4*>(qdst + q_offset<C::NQK>(RP + r, w16)) = make_uint4(t2w[0], t2w[1], t2w[2], t2w[3]);
-          };
-          emit(v, lane);
-          if (lane < 4) emit(tail, 32 + lane);
-        }
-      }
+      stage_rows<RP>(p, R, ms->row_off, qseq, qdst, row_scale, w2, 2, lane);
       fence_proxy_async_smem();
       mbar_arrive(&ms->q_full[slot]);
       ++k;
