@@ -20,8 +20,9 @@
 // Softmax is online over key tiles; one warpgroup owns one key per thread (its TMEM
 // lane), so the running max per row needs a cross-warp reduction each tile.
 //
-// Roles (256 threads): warp 0 issues TMA, warp 1 owns TMEM and issues MMAs, warps 4-7
-// stage queries, run the softmax and write the epilogue. Every wait is bounded.
+// Roles (384 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the score MMAs,
+// warp 3 issues the value MMAs, warp 2 stages query rows, warps 4-11 (two warpgroups)
+// run the softmax and write the epilogue. Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,13 +43,13 @@ constexpr int kStages = 2;
 constexpr int kChunkBytes = 16384;                     // 128 keys x 128 bytes, SW128
 constexpr int kTailOffset = 4 * kChunkBytes;            // 128 keys x 64 bytes, SW64
 constexpr int kStageBytes = kTailOffset + 2 * 4096;     // 73,728
-constexpr int kThreads = 384;  // producer, MMA, 2 query stagers, 2 softmax warpgroups
+constexpr int kThreads = 384;  // producer, 2 MMA issuers, query stager, 2 softmax warpgroups
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 4.0f;      // P carried as 2^(x - m + 4): at most 2^8 while x <= m + 4
 constexpr float kRescaleGap = 4.0f;  // the running max (log2 units) moves only past m + 4
-constexpr int kPrefetchTiles = 3;    // tiles the producer pulls into L2 ahead of its TMA loads
+constexpr int kPrefetchTiles = 1;    // tiles the producer pulls into L2 ahead of its TMA loads
 
 template <int RP>
 struct Cfg {
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ms->p_full, 256);
     mbar_init(&ms->pv_done, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&ms->q_full[s], 64);
+      mbar_init(&ms->q_full[s], 32);
       mbar_init(&ms->q_empty[s], 1);
     }
     mbar_init(&ms->q0_done, 320);
@@ -452,125 +453,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    // Two cursors over this CTA's tiles, polled without blocking: scores (QK) of tile g
-    // may run ahead while values (PV) of tile g-1 wait for their probabilities, and a PV
-    // is issued the moment its P is ready so its KV stage returns to the producer early.
+    // ------------------------------------------------------------------ scores issuer
+    // QK of every tile, as soon as its KV stage is full, its S^T buffer has been read and
+    // its unit's query terms are staged. Values (PV) have their own issuing warp: a single
+    // thread spends tens of cycles per tcgen05.mma, so one issuer would serialise the two.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, 128, C::NQK);
-      constexpr uint32_t idesc_pv = instr_desc(0, 0, 1, 1, 128, C::NPV);
-      const uint32_t q_s0 = smem_addr(qbuf), p_s = smem_addr(pbuf);
-      auto tiles_of = [&](int u) { return tiles_in(get_unit(args, num_units, u)); };
-      // next unit (from u on, stepping by the grid) that has at least one key tile
-      auto next_busy = [&](int u, int* n) {
-        while (u < u_end && (*n = tiles_of(u)) == 0) u += u_step;
-        return u;
-      };
-      // scores cursor
-      int qn = 0, qt = 0;
-      int qu = next_busy(u_begin, &qn);
-      uint32_t qg = 0, q_units = 0;
-      bool q_ready = false;
-      // values cursor
-      int pu = qu, pt = 0, pn = qn;
-      uint32_t pg = 0;
-      uint64_t idle_since = globaltimer_ns();
-      while (pu < u_end) {
-        bool progress = false;
-        // values first: a finished PV hands its KV stage back to the producer
-        if (pg < qg && mbar_test_wait(&ms->p_full, pg & 1)) {
+      const uint64_t a_main0 = smem_desc(smem_addr(smem + C::kOffStages), 16, 1024, Swizzle::k128B);
+      const uint64_t a_tail0 = smem_desc(smem_addr(smem + C::kOffStages + kTailOffset), 16, 512, Swizzle::k64B);
+      const uint64_t b_main0 = smem_desc(smem_addr(qbuf), 16, 1024, Swizzle::k128B);
+      const uint64_t b_tail0 = smem_desc(smem_addr(qbuf + 4 * (C::NQK * 128)), 16, 512, Swizzle::k64B);
+      uint32_t g = 0, units_done = 0;
+      bool ok = true;
+      for (int u = u_begin; u < u_end && ok; u += u_step) {
+        const int n = tiles_in(get_unit(args, num_units, u));
+        if (n == 0) continue;
+        const int qslot = units_done % C::kQB;
+        if (!(ok = wait_or_abort(&ms->q_full[qslot], (units_done / C::kQB) & 1, ms, p))) break;
+        const uint32_t qoff = (uint32_t)(qslot * C::kQBytes) >> 4;
+        for (int t = 0; t < n; ++t, ++g) {
+          const int s = g % kStages, sb = g & 1;
+          if (!(ok = wait_or_abort(&ms->kv_full[s], (g / kStages) & 1, ms, p))) break;
+          if (!(ok = wait_or_abort(&ms->s_empty[sb], ((g >> 1) & 1) ^ 1, ms, p))) break;
           tc_fence_after();
-          const int s = pg % kStages;
-          const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
-          const bool first = (pt == 0);
+          const uint32_t soff = (uint32_t)(s * kStageBytes) >> 4;
+          const uint32_t d = tmem + C::kSCol + sb * C::NQK;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8f6f4(d, a_main0 + soff + ((c * kChunkBytes + kk * 32) >> 4),
+                         b_main0 + qoff + ((c * (C::NQK * 128) + kk * 32) >> 4), idesc_qk,
+                         (c | kk) != 0);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma_f8f6f4(d, a_tail0 + soff + ((kk * 32) >> 4), b_tail0 + qoff + ((kk * 32) >> 4),
+                       idesc_qk, 1);
+          mma_commit(&ms->s_full[sb]);
+        }
+        if (!ok) break;
+        mma_commit(&ms->q_empty[qslot]);  // that query buffer is free once these complete
+        ++units_done;
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------------ values issuer
+    // PV of every tile the moment its probabilities are in shared memory; completion hands
+    // the KV stage back to the producer and lets the softmax reuse P and rescale O.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = instr_desc(0, 0, 1, 1, 128, C::NPV);
+      const uint64_t a0 = smem_desc(smem_addr(smem + C::kOffStages), kChunkBytes, 1024, Swizzle::k128B);
+      const uint64_t b0 = smem_desc(smem_addr(pbuf), 128, 2048, Swizzle::kNone);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int u = u_begin; u < u_end && ok; u += u_step) {
+        const int n = tiles_in(get_unit(args, num_units, u));
+        for (int t = 0; t < n; ++t, ++g) {
+          if (!(ok = wait_or_abort(&ms->p_full, g & 1, ms, p))) break;
+          tc_fence_after();
+          const int s = g % kStages;
+          const uint32_t soff = (uint32_t)(s * kStageBytes) >> 4;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const uint32_t d = tmem + C::kOCol + c * C::OCOLS;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t a = smem_desc(st + c * kChunkBytes + ks * 4096, kChunkBytes, 1024, Swizzle::k128B);
+              const uint64_t a = a0 + soff + ((c * kChunkBytes + ks * 4096) >> 4);
               if (C::kStackP) {
-                const uint64_t b = smem_desc(p_s + ks * 512, 128, 2048, Swizzle::kNone);
-                mma_f8f6f4(d, a, b, idesc_pv, !first || ks > 0);
+                mma_f8f6f4(d, a, b0 + ((ks * 512) >> 4), idesc_pv, t > 0 || ks > 0);
               } else {
 #pragma unroll
-                for (int term = 0; term < 3; ++term) {
-                  const uint64_t b = smem_desc(p_s + term * (RP / 16) * 2048 + ks * 512, 128, 2048, Swizzle::kNone);
-                  mma_f8f6f4(d, a, b, idesc_pv, !first || ks > 0 || term > 0);
-                }
+                for (int term = 0; term < 3; ++term)
+                  mma_f8f6f4(d, a, b0 + ((term * (RP / 16) * 2048 + ks * 512) >> 4), idesc_pv,
+                             t > 0 || ks > 0 || term > 0);
               }
             }
           }
           mma_commit(&ms->kv_empty[s]);
           mma_commit(&ms->pv_done);
-          ++pg;
-          if (++pt == pn) {
-            pu += u_step;
-            pt = 0;
-            pu = next_busy(pu, &pn);
-          }
-          progress = true;
-        }
-        if (qu < u_end) {
-          const int s = qg % kStages, sb = qg & 1;
-          bool ready = true;
-          const int qslot = q_units % C::kQB;
-          if (qt == 0 && !q_ready) {
-            q_ready = mbar_test_wait(&ms->q_full[qslot], (q_units / C::kQB) & 1);
-            ready = q_ready;
-          }
-          ready = ready && mbar_test_wait(&ms->kv_full[s], (qg / kStages) & 1) &&
-                  mbar_test_wait(&ms->s_empty[sb], ((qg >> 1) & 1) ^ 1);
-          if (ready) {
-            tc_fence_after();
-            const uint32_t st = smem_addr(smem + C::kOffStages + s * kStageBytes);
-            const uint32_t d = tmem + C::kSCol + sb * C::NQK;
-            const uint32_t q_s = q_s0 + qslot * C::kQBytes;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = smem_desc(st + c * kChunkBytes + kk * 32, 16, 1024, Swizzle::k128B);
-                const uint64_t b = smem_desc(q_s + c * (C::NQK * 128) + kk * 32, 16, 1024, Swizzle::k128B);
-                mma_f8f6f4(d, a, b, idesc_qk, (c | kk) != 0);
-              }
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const uint64_t a = smem_desc(st + kTailOffset + kk * 32, 16, 512, Swizzle::k64B);
-              const uint64_t b = smem_desc(q_s + 4 * (C::NQK * 128) + kk * 32, 16, 512, Swizzle::k64B);
-              mma_f8f6f4(d, a, b, idesc_qk, 1);
-            }
-            mma_commit(&ms->s_full[sb]);
-            ++qg;
-            if (++qt == qn) {
-              mma_commit(&ms->q_empty[qslot]);  // that query buffer is free once these complete
-              qu += u_step;
-              qt = 0;
-              q_ready = false;
-              ++q_units;
-              qu = next_busy(qu, &qn);
-            }
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle_since = globaltimer_ns();
-        } else if (globaltimer_ns() - idle_since > kWaitLimitNs || aborted(ms)) {
-          ms->abort = 1;
-          report(p.hdr, MLA_ERR_TIMEOUT);
-          break;
-        } else {
-          __nanosleep(40);  // leave the issue slots to the softmax warp on this SMSP
         }
       }
     }
-  } else if (warp == 2 || warp == 3) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------------ query stager
     // Each unit's query rows go into the query operand as two e4m3 terms with a per-row
     // power-of-two scale, as soon as the previous unit's scores stopped reading it; the
     // softmax warps meanwhile finish the previous unit.
-    const int w2 = warp - 2;
-    const float kv_scale = p.kv_scale;
     uint32_t k = 0;  // units with work, in order
     for (int u = u_begin; u < u_end; u += u_step) {
       const UnitInfo ui = get_unit(args, num_units, u);
@@ -587,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* qdst = qbuf + slot * C::kQBytes;
       float* row_scale = ms->row_scale[k & 1];
       const uint16_t* qseq = p.q + (int64_t)ui.qrow0 * kD;
-      stage_rows<RP>(p, R, ms->row_off, qseq, qdst, row_scale, w2, 2, lane);
+      stage_rows<RP>(p, R, ms->row_off, qseq, qdst, row_scale, 0, 1, lane);
       fence_proxy_async_smem();
       mbar_arrive(&ms->q_full[slot]);
       ++k;
