@@ -84,9 +84,12 @@ typedef struct mla_kv {
 
 /*
  * Bytes of workspace the given call needs on `device` (a CUDA ordinal). The workspace
- * holds the split plan, the per-split partial outputs and the status word; it must be
- * 256-byte aligned and stay untouched until the call's work has finished on its stream.
- * For MLA_OP_PREFILL pass B = 1 and n_q = T. Returns 0 for unsupported arguments.
+ * holds each sequence's place in the split plan, the per-split partial outputs and one
+ * status word per CTA; it must be 256-byte aligned and stay untouched until the call's
+ * work has finished on its stream. Its contents need no initialisation: every call
+ * rewrites all it later reads (zero-fill it once if mla_read_status may run before the
+ * first call). For MLA_OP_PREFILL pass B = 1 and n_q = T. Returns 0 for unsupported
+ * arguments.
  */
 size_t mla_workspace_size(mla_op_t op, int B, int H, int n_q, int device);
 
@@ -143,9 +146,9 @@ mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, 
                            void* out, float* lse, void* stream);
 
 /*
- * Synchronises `stream`, then returns the status word the last call on this workspace
- * left (MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT), or MLA_ERR_CUDA if the stream itself
- * reports an error. Each compute call resets the word when its work starts.
+ * Synchronises `stream`, then returns the status the last call on this workspace left
+ * (MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT: the first non-zero of the words its CTAs
+ * wrote at exit), or MLA_ERR_CUDA if the stream itself reports an error.
  */
 mla_status_t mla_read_status(const void* workspace, size_t workspace_bytes, void* stream);
 
@@ -176,12 +179,13 @@ void mla_set_profile_events(void* start, void* stop);
  * by this call.
  *  - A batch whose mla_workspace_size(MLA_OP_DECODE, B, H, 1, device) exceeds
  *    MLA_STATIC_WS_BYTES is rejected with MLA_ERR_WORKSPACE before anything is enqueued
- *    (16 MiB covers, for example, 32 sequences x 16 heads on a 152-SM GB300).
+ *    (16 MiB covers 16-head decode of any batch up to several hundred thousand
+ *    sequences on a 152-SM GB300: the partial outputs take about 10 MB of it).
  *  - The first call on each device looks up the array's device address (a runtime
  *    symbol query); make that first call outside any CUDA stream capture.
  *  - All calls on a device share the one array, which keeps the previous call's
- *    contents (each call re-plans and overwrites what it reads, and resets its status
- *    word). Calls whose work overlaps on the GPU (different streams without ordering,
+ *    contents (each call rewrites everything it reads). Calls whose work overlaps on
+ *    the GPU (different streams without ordering,
  *    or several host threads) race on it and give wrong results: serialise them.
  *  - The device-side status word of these calls cannot be read with mla_read_status.
  */

@@ -134,11 +134,11 @@ def mla_workspace_size(op: int, B: int, H: int, n_q: int, device: Optional[int] 
 
 
 def workspace(op: int, B: int, H: int, n_q: int, device=None) -> torch.Tensor:
-    """A uint8 device buffer of the size mla_workspace_size() asks for."""
+    """A zero-filled uint8 device buffer of the size mla_workspace_size() asks for."""
     n = mla_workspace_size(op, B, H, n_q, None if device is None else torch.device(device).index)
     if n == 0:
         raise ValueError("unsupported arguments for mla_workspace_size")
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def _q_check(q: torch.Tensor, ndim: int) -> None:

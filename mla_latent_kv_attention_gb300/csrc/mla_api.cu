@@ -85,17 +85,14 @@ mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
   mla::AttnParams p = base_params(kv, q, B, n_q, H, sm_scale, out, lse);
   char* base = static_cast<char*>(ws);
   p.hdr = reinterpret_cast<mla::WsHeader*>(base + w.hdr);
-  p.units = reinterpret_cast<mla::Unit*>(base + w.units);
-  p.seqs = reinterpret_cast<mla::SeqUnits*>(base + w.seqs);
+  p.status = reinterpret_cast<unsigned*>(base + w.status);
+  p.seqs = reinterpret_cast<mla::SeqSpan*>(base + w.seqs);
   p.part_lse = reinterpret_cast<float*>(base + w.part_lse);
   p.part_out = reinterpret_cast<float*>(base + w.part_out);
-  p.cta_first = reinterpret_cast<int*>(base + w.cta_first);
-  p.blk_prefix = reinterpret_cast<int*>(base + w.blk_prefix);
-  p.max_units = w.max_units;
+  p.qimg = reinterpret_cast<uint8_t*>(base + w.qimg);
+  p.qimg_stride = (int64_t)w.qimg_stride;
   p.num_ctas = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mla::launch_plan(p, s) != cudaSuccess) return MLA_ERR_CUDA;
-  ++g_last_launches;
   prof_mark(g_prof_start, s);
   int launched = 0;
   const cudaError_t e = mla::launch_decode_tc(p, sms, s, &launched);
@@ -118,7 +115,8 @@ size_t mla_workspace_size(mla_op_t op, int B, int H, int n_q, int device) {
   if (H < 1 || H > MLA_MAX_HEADS || B < 0) return 0;
   if (op == MLA_OP_PREFILL) {
     if (B != 1 || n_q < 0) return 0;
-    return sizeof(mla::WsHeader);
+    const int sms = sm_count(device);
+    return sms > 0 ? mla::ws_prefill_bytes(sms) : 0;
   }
   if (op == MLA_OP_DECODE) n_q = 1;
   if (n_q < 1 || n_q > MLA_MAX_NQ) return 0;
@@ -156,11 +154,15 @@ mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float 
   if ((st = current_device(&dev)) != MLA_OK) return st;
   const int sms = sm_count(dev);
   if (sms <= 0) return MLA_ERR_CUDA;
+  if (workspace_bytes < mla::ws_prefill_bytes(sms)) return MLA_ERR_WORKSPACE;
   mla::AttnParams p = base_params(kv, q, 1, T, H, sm_scale, out, lse);
-  p.hdr = static_cast<mla::WsHeader*>(workspace);
+  char* base = static_cast<char*>(workspace);
+  p.hdr = reinterpret_cast<mla::WsHeader*>(base);
+  p.status = reinterpret_cast<unsigned*>(base + mla::ws_prefill_status(sms));
+  p.qimg = reinterpret_cast<uint8_t*>(base + mla::ws_prefill_qimg(sms));
+  p.qimg_stride = (int64_t)mla::qimg_bytes(48);
+  p.num_ctas = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mla::launch_reset_status(p.hdr, s) != cudaSuccess) return MLA_ERR_CUDA;
-  ++g_last_launches;
   prof_mark(g_prof_start, s);
   int launched = 0;
   const cudaError_t e = mla::launch_prefill_tc(p, sms, s, &launched);
@@ -183,7 +185,12 @@ mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, 
       (lse && !aligned(lse, 4)))
     return MLA_ERR_INVALID_ARG;
   if (R > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
-  if (mla::launch_merge_standalone(part_out, part_lse, S, R, static_cast<uint16_t*>(out), lse,
+  int dev;
+  mla_status_t st = current_device(&dev);
+  if (st != MLA_OK) return st;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return MLA_ERR_CUDA;
+  if (mla::launch_merge_standalone(part_out, part_lse, S, R, static_cast<uint16_t*>(out), lse, sms,
                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
   ++g_last_launches;
@@ -193,13 +200,27 @@ mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, 
 mla_status_t mla_read_status(const void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < sizeof(mla::WsHeader)) return MLA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned int word = 0;
-  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+  mla::WsHeader h;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }
-  return static_cast<mla_status_t>(word);
+  // one word per CTA of the last launch, right after the header; the first error wins
+  const size_t off = mla::align_up(sizeof(mla::WsHeader), 256);
+  if (h.num_ctas < 0 || h.num_ctas > 4096 || off + sizeof(unsigned) * (size_t)h.num_ctas > workspace_bytes)
+    return MLA_ERR_WORKSPACE;
+  if (h.num_ctas == 0) return MLA_OK;
+  unsigned words[4096];
+  if (cudaMemcpyAsync(words, static_cast<const char*>(workspace) + off,
+                      sizeof(unsigned) * (size_t)h.num_ctas, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  for (int c = 0; c < h.num_ctas; ++c)
+    if (words[c] != 0) return static_cast<mla_status_t>(words[c]);
+  return MLA_OK;
 }
 
 const char* mla_status_string(mla_status_t status) {

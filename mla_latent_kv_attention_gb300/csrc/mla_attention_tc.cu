@@ -89,9 +89,16 @@ struct Misc {
   uint64_t q_full[2];   // query operand buffer holds its unit's terms
   uint64_t q_empty[2];  // the unit that used the buffer has finished its scores
   uint64_t q0_done;     // the first unit's query rows are staged (by warps 2-11 together)
+  uint64_t q1_done;     // the second unit's rows are in this CTA's global query image
   uint64_t wg_bar[2];  // bounded barriers of the two softmax warpgroups (128 arrivals)
+  // decode/verify split plan of this CTA: blocks [x0, x1) of all sequences end to end;
+  // the range begins in sequence b0, whose first block is pre0
+  long long plan_x0, plan_x1, plan_pre0;
+  int plan_b0, plan_L0;  // ... and b0's length
+  int scan[kThreads / 32];
   uint32_t tmem_base;
   int abort;
+  unsigned status;  // this CTA's first error
 };
 static_assert(offsetof(Misc, row_scale) % 16 == 0 && offsetof(Misc, red) % 16 == 0 &&
                   offsetof(Misc, lred) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0,
@@ -107,18 +114,30 @@ struct DecodeArgs {
   AttnParams p;
   int h0, Hs;  // heads [h0, h0 + Hs) handled by this launch
   int rows;    // rows per unit: n_q * Hs (decode/verify) or P * H (prefill), <= RP
-  int prefill;    // 1: units are blocks of P new positions of one sequence (no planner)
+  int prefill;    // 1: units are blocks of P new positions of one sequence (no split plan)
   int P;          // prefill: new positions per unit
   int num_units;  // prefill: ceil(n_q / P)
+  int status_overwrite;  // 1: each CTA writes its status word even when clean (first launch)
 };
 
 // One unit of work as every role of the kernel sees it.
 struct UnitInfo {
   int b, key_lo, key_hi;
+  int L;          // cached positions of sequence b
   int qrow0;      // global row (of q, out, lse) of the unit's row 0
   int j0;         // new-position index of the unit's first position
   int rows;       // valid rows of the unit
   int final_out;  // 1: bf16 out + lse directly; 0: normalised partial for the merge
+  int slot;       // partial slot (when final_out == 0)
+};
+
+// Position in this CTA's list of units. Decode/verify: the sequences that overlap the CTA's
+// block range, in order (b, its first block pre, its length L). Prefill: unit index u.
+struct Cursor {
+  int u;
+  int b;
+  long long pre;
+  int L;
 };
 
 __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
@@ -129,30 +148,65 @@ __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
   return L;
 }
 
-__device__ __forceinline__ UnitInfo get_unit(const DecodeArgs& a, int num_units, int u) {
+__device__ __forceinline__ int blocks_of(int L) { return (L + kKeyBlock - 1) / kKeyBlock; }
+
+__device__ __forceinline__ Cursor first_unit(const DecodeArgs& a, const Misc* ms) {
+  Cursor c;
+  c.u = blockIdx.x;
+  c.b = ms->plan_b0;
+  c.pre = ms->plan_pre0;
+  c.L = ms->plan_L0;
+  return c;
+}
+
+__device__ __forceinline__ bool has_unit(const DecodeArgs& a, const Misc* ms, const Cursor& c) {
+  return a.prefill ? c.u < a.num_units : (c.b < a.p.B && c.pre < ms->plan_x1);
+}
+
+// The next unit: the next sequence with at least one key (decode/verify), or the next
+// unit index this CTA owns (prefill).
+__device__ __forceinline__ Cursor next_unit(const DecodeArgs& a, Cursor c) {
+  if (a.prefill) {
+    c.u += gridDim.x;
+    return c;
+  }
+  c.pre += blocks_of(c.L);
+  do {
+    ++c.b;
+    c.L = (c.b < a.p.B) ? seq_len_of(a.p, c.b) : 0;
+  } while (c.b < a.p.B && c.L == 0);
+  return c;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, const Misc* ms, const Cursor& c) {
   const AttnParams& p = a.p;
   UnitInfo x;
   if (!a.prefill) {
-    const Unit un = p.units[u];
-    x.b = un.b;
-    x.key_lo = un.key_lo;
-    x.key_hi = un.key_hi;
-    x.qrow0 = un.b * p.R;
+    const long long nb = blocks_of(c.L);
+    const long long blo = max(ms->plan_x0, c.pre), bhi = min(ms->plan_x1, c.pre + nb);
+    x.b = c.b;
+    x.L = c.L;
+    x.key_lo = (int)(blo - c.pre) * kKeyBlock;
+    x.key_hi = (bhi > blo) ? min(c.L, (int)(bhi - c.pre) * kKeyBlock) : x.key_lo;
+    x.qrow0 = c.b * p.R;
     x.j0 = 0;
     x.rows = a.rows;
-    x.final_out = p.seqs[un.b].count == 1;
+    x.final_out = (blo == c.pre && bhi == c.pre + nb);
+    x.slot = 2 * (int)blockIdx.x + (blo == ms->plan_x0 ? 0 : 1);
   } else {
     // the last positions see the most keys: hand those out first
-    const int pos0 = (num_units - 1 - u) * a.P;
+    const int pos0 = (a.num_units - 1 - c.u) * a.P;
     const int npos = min(a.P, p.n_q - pos0);
     const int L = seq_len_of(p, 0);
     x.b = 0;
+    x.L = L;
     x.key_lo = 0;
     x.key_hi = max(0, min(L, L - p.n_q + pos0 + npos));  // last key the unit's last position sees, + 1
     x.qrow0 = pos0 * p.H;
     x.j0 = pos0;
     x.rows = npos * p.H;
     x.final_out = 1;
+    x.slot = 0;
   }
   return x;
 }
@@ -161,11 +215,16 @@ __device__ __forceinline__ int tiles_in(const UnitInfo& x) {
   return (x.key_hi - x.key_lo + kTileKeys - 1) / kTileKeys;
 }
 
+// First error of this CTA wins; the CTA writes it to its status word at exit.
+__device__ __forceinline__ void report(Misc* m, mla_status_t code) {
+  atomicCAS(&m->status, 0u, (unsigned)code);
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Misc* m,
                                               const AttnParams& p) {
   if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
   m->abort = 1;
-  report(p.hdr, MLA_ERR_TIMEOUT);
+  report(m, MLA_ERR_TIMEOUT);
   return false;
 }
 
@@ -340,11 +399,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ms->p_full, 256);
     mbar_init(&ms->pv_done, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&ms->q_full[s], 32);
+      mbar_init(&ms->q_full[s], 1);
       mbar_init(&ms->q_empty[s], 1);
     }
     mbar_init(&ms->q0_done, 320);
+    mbar_init(&ms->q1_done, 320);
     ms->abort = 0;
+    ms->status = 0;
+    ms->plan_b0 = args.p.B;  // no unit unless the plan finds one
+    ms->plan_x0 = ms->plan_x1 = ms->plan_pre0 = 0;
+    ms->plan_L0 = 0;
     for (int r = 0; r < 48; ++r) {
       ms->row_j[r] = (r < args.rows) ? r / args.Hs : -(1 << 30);
       ms->row_off[r] = (r < args.rows) ? (r / args.Hs) * p.H + args.h0 + r % args.Hs : 0;
@@ -358,28 +422,113 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
-  // Everything above overlapped the planner (programmatic dependent launch); from here on
-  // the plan is read. The merge kernel may launch early and waits for this grid itself.
+  // Everything above may overlap the previous kernel in the stream (programmatic dependent
+  // launch); inputs are read only after it has completed. The merge kernel, a programmatic
+  // dependent of this one, may be scheduled from here on and waits for this grid itself.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int num_units = args.prefill ? args.num_units : p.hdr->num_units;
-  // this CTA's units: a contiguous range from the planner (decode/verify), or every
-  // gridDim.x-th unit (prefill)
-  const int u_begin = args.prefill ? (int)blockIdx.x : p.cta_first[blockIdx.x];
-  const int u_end = args.prefill ? num_units : p.cta_first[blockIdx.x + 1];
-  const int u_step = args.prefill ? (int)gridDim.x : 1;
 
-  // The first unit's queries are on every CTA's critical path: warps 2-11 stage them
-  // together (about two rows each); the two stager warps then run ahead for later units.
+  if (!args.prefill) {
+    // ---- split plan (decode/verify), computed by every CTA for itself. The 128-key blocks
+    // of all sequences, laid end to end, are cut into gridDim.x nearly equal contiguous
+    // ranges; this CTA owns [x0, x1), one unit per sequence the range overlaps. A long
+    // history thus spreads over every SM ("Scaling Kimi K3 on AMD Instinct MI355X", section
+    // "并行度必须适配真正的形状": hand the long history to more work groups), a batch of
+    // short sequences stays one unit per sequence, and a sequence is split only where a
+    // range boundary falls inside it.
+    const int B = p.B, tid = threadIdx.x;
+    const int per = (B + kThreads - 1) / kThreads;  // sequences per thread, contiguous
+    const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+    long long mine = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+      const int L = p.seq_lens[b];
+      const int64_t cap = p.pt_stride * (int64_t)p.page_size;
+      if (L < 0 || (int64_t)L > cap) report(ms, MLA_ERR_BOUNDS);
+      mine += blocks_of(seq_len_of(p, b));
+    }
+    // exclusive prefix of the per-thread block counts over the CTA
+    long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) ms->scan[warp] = (int)incl;
+    __syncthreads();
+    long long before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) before += ms->scan[w];
+      total += ms->scan[w];
+    }
+    long long pre = before + incl - mine;
+    const long long n = gridDim.x, c = blockIdx.x;
+    const long long x0 = total > 0 ? range_lo(c, total, n) : 0;
+    const long long x1 = total > 0 ? range_lo(c + 1, total, n) : 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+      const int nb = blocks_of(seq_len_of(p, b));
+      if (nb > 0 && pre <= x0 && x0 < pre + nb && x0 < x1) {
+        ms->plan_b0 = b;
+        ms->plan_pre0 = pre;
+        ms->plan_L0 = seq_len_of(p, b);
+      }
+      if (b % (int)n == (int)c) p.seqs[b] = SeqSpan{(int)pre, nb};
+      pre += nb;
+    }
+    if (tid == 0) {
+      ms->plan_x0 = x0;
+      ms->plan_x1 = x1;
+      if (c == 0) p.hdr->total_blocks = (int)total;
+    }
+    __syncthreads();
+    // Ask L2 for the first unit's query rows and page-table entries before the first TMA
+    // loads go out: behind the initial burst of key traffic they would arrive late, and
+    // both are on the path to the first scores.
+    if (warp >= 2 && ms->plan_b0 < B) {
+      const int b0 = ms->plan_b0;
+      const int t = threadIdx.x - 64;  // 320 threads
+      const int qlines = args.rows * 9;  // 1,152 bytes per row
+      if (t < qlines)
+        prefetch_l2(reinterpret_cast<const uint8_t*>(
+                        p.q + ((int64_t)b0 * p.R + ms->row_off[t / 9]) * kD) + (t % 9) * 128);
+      // and the second unit's rows (its sequence follows b0) for the prologue's second pass
+      const Cursor c1 = next_unit(args, first_unit(args, ms));
+      if (t < qlines && has_unit(args, ms, c1))
+        prefetch_l2(reinterpret_cast<const uint8_t*>(
+                        p.q + ((int64_t)c1.b * p.R + ms->row_off[t / 9]) * kD) + (t % 9) * 128);
+      const int64_t pg0 = (ms->plan_x0 - ms->plan_pre0) * kKeyBlock / p.page_size;
+      const int64_t pg = pg0 + (int64_t)(t - 304) * 32;  // four lines of 32 entries
+      if (t >= 304 && t < 304 + 4 && pg < p.pt_stride)
+        prefetch_l2(p.page_table + (int64_t)b0 * p.pt_stride + pg);
+    }
+    __syncthreads();
+  }
+
+  // The first unit's queries are on every CTA's critical path: warps 2-11 stage them into
+  // shared memory together (about two rows each). Later units' rows go to this CTA's query
+  // image in global memory and reach shared memory in one bulk copy when their unit starts
+  // (staging takes one warp far longer than a unit boundary may last): warps 2-11 stage the
+  // second unit there before the first key tile lands, the stager warp each later one while
+  // the unit before it runs.
   if (warp >= 2) {
-    int u0 = u_begin;
-    while (u0 < u_end && tiles_in(get_unit(args, num_units, u0)) == 0) u0 += u_step;
-    if (u0 < u_end) {
-      const UnitInfo ui = get_unit(args, num_units, u0);
+    Cursor c0 = first_unit(args, ms);
+    while (has_unit(args, ms, c0) && tiles_in(unit_info(args, ms, c0)) == 0) c0 = next_unit(args, c0);
+    if (has_unit(args, ms, c0)) {
+      const UnitInfo ui = unit_info(args, ms, c0);
       stage_rows<RP>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, qbuf,
                      ms->row_scale[0], warp - 2, 10, lane);
       fence_proxy_async_smem();
       mbar_arrive(&ms->q0_done);
+      Cursor c1 = next_unit(args, c0);
+      while (has_unit(args, ms, c1) && tiles_in(unit_info(args, ms, c1)) == 0) c1 = next_unit(args, c1);
+      if (has_unit(args, ms, c1)) {
+        const UnitInfo u1 = unit_info(args, ms, c1);
+        uint8_t* img = p.qimg + (int64_t)blockIdx.x * p.qimg_stride;
+        stage_rows<RP>(p, u1.rows, ms->row_off, p.q + (int64_t)u1.qrow0 * kD, img,
+                       reinterpret_cast<float*>(img + C::kQBytes), warp - 2, 10, lane);
+        fence_proxy_async_global();
+        mbar_arrive(&ms->q1_done);
+      }
     }
   }
 
@@ -391,15 +540,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fill = 0;  // tiles issued so far
       // L2 prefetch cursor: runs kPrefetchTiles tiles ahead of the TMA loads so that they
       // find their pages in L2 (deeper than the two shared-memory stages allow).
-      int pf_u = u_begin;
-      UnitInfo pu = (pf_u < u_end) ? get_unit(args, num_units, pf_u) : UnitInfo{};
+      Cursor pf_c = first_unit(args, ms);
+      UnitInfo pu = has_unit(args, ms, pf_c) ? unit_info(args, ms, pf_c) : UnitInfo{};
       int pf_k = pu.key_lo;
       uint32_t pf_tiles = 0;
       auto prefetch_upto = [&](uint32_t target) {
-        while (pf_tiles < target && pf_u < u_end) {
+        while (pf_tiles < target && has_unit(args, ms, pf_c)) {
           if (pf_k >= pu.key_hi) {  // unit done (or empty)
-            pf_u += u_step;
-            if (pf_u < u_end) pu = get_unit(args, num_units, pf_u);
+            pf_c = next_unit(args, pf_c);
+            if (has_unit(args, ms, pf_c)) pu = unit_info(args, ms, pf_c);
             pf_k = pu.key_lo;
             continue;
           }
@@ -418,8 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf_k += kTileKeys;
         }
       };
-      for (int u = u_begin; u < u_end && !aborted(ms); u += u_step) {
-        const UnitInfo un = get_unit(args, num_units, u);
+      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && !aborted(ms);
+           cu = next_unit(args, cu)) {
+        const UnitInfo un = unit_info(args, ms, cu);
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
           const int s = fill % kStages;
           const uint32_t n = fill / kStages;
@@ -436,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (phys >= 0 && phys < p.num_pages)
                 y = phys * p.page_size + (kk % p.page_size);
               else
-                report(p.hdr, MLA_ERR_BOUNDS);
+                report(ms, MLA_ERR_BOUNDS);
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -465,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t b_tail0 = smem_desc(smem_addr(qbuf + 4 * (C::NQK * 128)), 16, 512, Swizzle::k64B);
       uint32_t g = 0, units_done = 0;
       bool ok = true;
-      for (int u = u_begin; u < u_end && ok; u += u_step) {
-        const int n = tiles_in(get_unit(args, num_units, u));
+      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && ok; cu = next_unit(args, cu)) {
+        const int n = tiles_in(unit_info(args, ms, cu));
         if (n == 0) continue;
         const int qslot = units_done % C::kQB;
         if (!(ok = wait_or_abort(&ms->q_full[qslot], (units_done / C::kQB) & 1, ms, p))) break;
@@ -506,26 +656,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t b0 = smem_desc(smem_addr(pbuf), 128, 2048, Swizzle::kNone);
       uint32_t g = 0;
       bool ok = true;
-      for (int u = u_begin; u < u_end && ok; u += u_step) {
-        const int n = tiles_in(get_unit(args, num_units, u));
+      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && ok; cu = next_unit(args, cu)) {
+        const int n = tiles_in(unit_info(args, ms, cu));
         for (int t = 0; t < n; ++t, ++g) {
           if (!(ok = wait_or_abort(&ms->p_full, g & 1, ms, p))) break;
           tc_fence_after();
           const int s = g % kStages;
           const uint32_t soff = (uint32_t)(s * kStageBytes) >> 4;
+          // consecutive MMAs go to different dv chunks' accumulators
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t d = tmem + C::kOCol + c * C::OCOLS;
+          for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t a = a0 + soff + ((c * kChunkBytes + ks * 4096) >> 4);
-              if (C::kStackP) {
-                mma_f8f6f4(d, a, b0 + ((ks * 512) >> 4), idesc_pv, t > 0 || ks > 0);
-              } else {
+            for (int term = 0; term < (C::kStackP ? 1 : 3); ++term) {
 #pragma unroll
-                for (int term = 0; term < 3; ++term)
-                  mma_f8f6f4(d, a, b0 + ((term * (RP / 16) * 2048 + ks * 512) >> 4), idesc_pv,
-                             t > 0 || ks > 0 || term > 0);
+              for (int c = 0; c < 4; ++c) {
+                const uint32_t d = tmem + C::kOCol + c * C::OCOLS;
+                const uint64_t a = a0 + soff + ((c * kChunkBytes + ks * 4096) >> 4);
+                const uint64_t b = b0 + ((term * (RP / 16) * 2048 + ks * 512) >> 4);
+                mma_f8f6f4(d, a, b, idesc_pv, t > 0 || ks > 0 || term > 0);
               }
             }
           }
@@ -540,24 +688,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // power-of-two scale, as soon as the previous unit's scores stopped reading it; the
     // softmax warps meanwhile finish the previous unit.
     uint32_t k = 0;  // units with work, in order
-    for (int u = u_begin; u < u_end; u += u_step) {
-      const UnitInfo ui = get_unit(args, num_units, u);
+    uint8_t* img = p.qimg + (int64_t)blockIdx.x * p.qimg_stride;
+    constexpr uint32_t kImgBytes = C::kQBytes + 48 * sizeof(float);
+    for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu); cu = next_unit(args, cu)) {
+      const UnitInfo ui = unit_info(args, ms, cu);
       if (tiles_in(ui) == 0) continue;
-      const int R = ui.rows;
       const int slot = k % C::kQB;
-      if (k == 0) {  // staged by warps 2-11 in the prologue
+      if (k == 0) {  // staged into shared memory by warps 2-11 in the prologue
         if (!wait_or_abort(&ms->q0_done, 0, ms, p)) break;
-        mbar_arrive(&ms->q_full[0]);
+        if (lane == 0) mbar_arrive(&ms->q_full[0]);
         ++k;
         continue;
       }
+      if (k == 1) {  // staged into the image by warps 2-11 in the prologue
+        if (!wait_or_abort(&ms->q1_done, 0, ms, p)) break;
+      } else {
+        // the image is free once the previous unit's copy out of it has landed
+        const uint32_t pk = k - 1;
+        if (!wait_or_abort(&ms->q_full[pk % C::kQB], (pk / C::kQB) & 1, ms, p)) break;
+        stage_rows<RP>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, img,
+                       reinterpret_cast<float*>(img + C::kQBytes), 0, 1, lane);
+        fence_proxy_async_global();
+        __syncwarp();
+      }
       if (k >= (uint32_t)C::kQB && !wait_or_abort(&ms->q_empty[slot], ((k / C::kQB) - 1) & 1, ms, p)) break;
-      uint8_t* qdst = qbuf + slot * C::kQBytes;
-      float* row_scale = ms->row_scale[k & 1];
-      const uint16_t* qseq = p.q + (int64_t)ui.qrow0 * kD;
-      stage_rows<RP>(p, R, ms->row_off, qseq, qdst, row_scale, 0, 1, lane);
-      fence_proxy_async_smem();
-      mbar_arrive(&ms->q_full[slot]);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ms->q_full[slot], kImgBytes);
+        bulk_g2s(qbuf + slot * C::kQBytes, img, C::kQBytes, &ms->q_full[slot]);
+        bulk_g2s(ms->row_scale[k & 1], img + C::kQBytes, 48 * sizeof(float), &ms->q_full[slot]);
+      }
+      __syncwarp();
       ++k;
     }
   } else if (warp >= kSoftmaxWarp0) {
@@ -581,8 +741,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return good;
     };
     bool ok = true;
-    for (int u = u_begin; u < u_end && ok; u += u_step) {
-      const UnitInfo un = get_unit(args, num_units, u);
+    for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && ok; cu = next_unit(args, cu)) {
+      const UnitInfo un = unit_info(args, ms, cu);
       const int R = un.rows;
       const int ntiles = tiles_in(un);
       const bool final_out = un.final_out != 0;
@@ -593,21 +753,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int dv = i; dv < kDV; dv += 128) p.out[row * kDV + dv] = 0;
             if (i == 0 && p.lse) p.lse[row] = -INFINITY;
           } else if (i == 0) {
-            p.part_lse[(int64_t)u * p.R + ms->row_off[r]] = -INFINITY;
+            p.part_lse[(int64_t)un.slot * p.R + ms->row_off[r]] = -INFINITY;
           }
         }
         continue;
       }
-      const int L = seq_len_of(p, un.b);
-      if (wg == 0) {  // warm L2 with the next unit's query rows (9 lines of 128 bytes per row)
-        const int un_next = u + u_step;
-        if (un_next < u_end) {
-          const UnitInfo nx = get_unit(args, num_units, un_next);
-          if (nx.qrow0 != un.qrow0)
-            for (int x = i; x < nx.rows * 9; x += 128)
-              prefetch_l2(reinterpret_cast<const uint8_t*>(p.q + ((int64_t)nx.qrow0 + ms->row_off[x / 9]) * kD) + (x % 9) * 128);
-        }
-      }
+      const int L = un.L;
       // last visible key of new position j is L - n_q + j (and the unit ends at key_hi)
       const int lim_cap = un.key_hi - 1;
       const int lim0 = min(lim_cap, L - p.n_q + un.j0);
@@ -797,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.out[((int64_t)un.qrow0 + roff) * kDV + dv] =
                 __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv[r]));
           } else {
-            p.part_out[((int64_t)u * p.R + roff) * kDV + dv] = acc * inv[r];
+            p.part_out[((int64_t)un.slot * p.R + roff) * kDV + dv] = acc * inv[r];
           }
         }
       }
@@ -815,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (final_out) {
           if (p.lse) p.lse[(int64_t)un.qrow0 + roff] = lse;
         } else {
-          p.part_lse[(int64_t)u * p.R + roff] = lse;
+          p.part_lse[(int64_t)un.slot * p.R + roff] = lse;
         }
       }
       ++k;
@@ -827,6 +978,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // this CTA's status word (a later launch of the same call only adds errors)
+    if (args.status_overwrite || ms->status != 0) p.status[blockIdx.x] = ms->status;
+    if (blockIdx.x == 0 && args.status_overwrite) p.hdr->num_ctas = gridDim.x;
   }
 }
 
@@ -905,7 +1061,7 @@ cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensor
 cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches) {
   CUtensorMap mm, mt;
   if (!encode_pool_maps(p, &mm, &mt)) return cudaErrorInvalidValue;
-  const int grid = p.num_ctas;  // the planner cut the work into this many ranges
+  const int grid = p.num_ctas;  // the split plan cuts the blocks into this many ranges
   (void)num_sms;
   const int groups = (p.R > 48) ? 2 : 1;
   for (int gi = 0; gi < groups; ++gi) {
@@ -918,6 +1074,7 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
     a.prefill = 0;
     a.P = 0;
     a.num_units = 0;
+    a.status_overwrite = (gi == 0);
     cudaError_t e;
     if (a.rows <= 16)
       e = launch_rp<16>(a, mm, mt, grid, s);
@@ -933,7 +1090,7 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
 
 // Causal prefill of one sequence: units are blocks of P = 48 / H new positions (all their
 // heads, at most 48 rows) over every key they see, handed out longest first. No split of
-// the key axis (there are thousands of units), so no planner and no merge.
+// the key axis (there are thousands of units), so no split plan and no merge.
 cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches) {
   CUtensorMap mm, mt;
   if (!encode_pool_maps(p, &mm, &mt)) return cudaErrorInvalidValue;
@@ -944,6 +1101,7 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, 
   a.P = 48 / p.H;
   a.rows = a.P * p.H;
   a.prefill = 1;
+  a.status_overwrite = 1;
   a.num_units = (p.n_q + a.P - 1) / a.P;
   const int grid = min(num_sms, a.num_units);
   const cudaError_t e = launch_rp<48>(a, mm, mt, grid, s);

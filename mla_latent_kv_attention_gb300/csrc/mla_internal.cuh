@@ -15,53 +15,70 @@ constexpr int kMaxRows = MLA_MAX_HEADS * MLA_MAX_NQ;  // query rows per sequence
 
 // Workspace header at offset 0 (256 bytes).
 struct WsHeader {
-  unsigned int status;   // mla_status_t written by the device (first error wins)
-  int num_units;         // units the planner produced
-  int blocks_per_unit;   // key blocks (of kKeyBlock keys) per unit
-  int pad[61];
+  int num_ctas;      // CTAs of the last attention launch: status slots [0, num_ctas) are its
+  int total_blocks;  // decode/verify: 128-key blocks of all sequences, end to end
+  int pad[62];
 };
 
-// One unit of split-KV work: keys [key_lo, key_hi) of sequence b.
-struct Unit {
-  int b, key_lo, key_hi, slot;
-};
-
-// Per-sequence unit range.
-struct SeqUnits {
-  int first, count;
-};
-
-// Offsets of the workspace regions for one decode/verify call.
-struct WsLayout {
-  size_t hdr, units, seqs, cta_first, blk_prefix, part_lse, part_out, total;
-  int max_units, max_ctas;
+// A sequence's 128-key blocks in the flat block order of all sequences laid end to end.
+struct SeqSpan {
+  int first_block, num_blocks;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Query rows one attention launch handles per unit (padded): 16, 32 or 48. More than 48
+// rows per sequence run as two launches over halves of the heads.
+inline int padded_rows(int rows_per_seq) {
+  const int r = rows_per_seq > 48 ? (rows_per_seq + 1) / 2 : rows_per_seq;
+  return r <= 16 ? 16 : (r <= 32 ? 32 : 48);
+}
+
+// One CTA's staged query image in global memory: the query operand of a later unit (two
+// e4m3 terms of each padded row, in shared-memory layout) followed by the rows' score
+// scales, copied into shared memory in one bulk copy when the unit starts.
+inline size_t qimg_bytes(int rp) { return align_up((size_t)2 * rp * MLA_D + sizeof(float) * 48, 256); }
+
+// Offsets of the workspace regions for one call.
+//   status:   one word per CTA, written by that CTA at exit (0 or its first error)
+//   seqs:     [B] SeqSpan, for the merge
+//   qimg:     one staged query image per CTA
+//   part_*:   two partial slots per CTA (the first and the last unit of its block range
+//             are the only ones that can hold part of a sequence), R rows each
+struct WsLayout {
+  size_t hdr, status, seqs, qimg, part_lse, part_out, total;
+  size_t qimg_stride;
+  int max_slots;
+};
+
 inline WsLayout ws_layout(int B, int rows_per_seq, int num_sms) {
   WsLayout w;
-  // one contiguous block range per CTA, split only where a sequence ends: at most
-  // (CTAs + B - 1) pieces
-  w.max_ctas = num_sms;
-  w.max_units = num_sms + B;
+  w.max_slots = 2 * num_sms;
+  w.qimg_stride = qimg_bytes(padded_rows(rows_per_seq));
   size_t off = 0;
   w.hdr = off;
   off += sizeof(WsHeader);
-  w.units = off = align_up(off, 256);
-  off += sizeof(Unit) * (size_t)w.max_units;
+  w.status = off = align_up(off, 256);
+  off += sizeof(unsigned) * (size_t)num_sms;
+  w.qimg = off = align_up(off, 256);
+  off += w.qimg_stride * (size_t)num_sms;
   w.seqs = off = align_up(off, 256);
-  off += sizeof(SeqUnits) * (size_t)(B > 0 ? B : 1);
-  w.cta_first = off = align_up(off, 256);
-  off += sizeof(int) * (size_t)(num_sms + 1);
-  w.blk_prefix = off = align_up(off, 256);
-  off += sizeof(int) * (size_t)(B + 1);
+  off += sizeof(SeqSpan) * (size_t)(B > 0 ? B : 1);
   w.part_lse = off = align_up(off, 256);
-  off += sizeof(float) * (size_t)w.max_units * rows_per_seq;
+  off += sizeof(float) * (size_t)w.max_slots * rows_per_seq;
   w.part_out = off = align_up(off, 256);
-  off += sizeof(float) * (size_t)w.max_units * rows_per_seq * kDV;
+  off += sizeof(float) * (size_t)w.max_slots * rows_per_seq * kDV;
   w.total = align_up(off, 256);
   return w;
+}
+
+// Prefill: the header, the per-CTA status words and the per-CTA query images (48 rows).
+inline size_t ws_prefill_status(int) { return align_up(sizeof(WsHeader), 256); }
+inline size_t ws_prefill_qimg(int num_sms) {
+  return align_up(ws_prefill_status(num_sms) + sizeof(unsigned) * (size_t)num_sms, 256);
+}
+inline size_t ws_prefill_bytes(int num_sms) {
+  return ws_prefill_qimg(num_sms) + qimg_bytes(48) * (size_t)num_sms;
 }
 
 // Everything an attention kernel needs for one call.
@@ -78,28 +95,30 @@ struct AttnParams {
   int B, n_q, H, R;   // R = n_q * H rows per sequence
   uint16_t* out;      // [B][n_q][H][512]
   float* lse;         // [B][n_q][H] or null
-  float* part_out;    // [max_units][R][512]
-  float* part_lse;    // [max_units][R]
-  Unit* units;
-  SeqUnits* seqs;
-  int* cta_first;   // [num_ctas + 1]: CTA c owns units [cta_first[c], cta_first[c + 1])
-  int* blk_prefix;  // [B + 1]: first 128-key block of each sequence in the flat block order
+  float* part_out;    // [2 * num_ctas][R][512]
+  float* part_lse;    // [2 * num_ctas][R]
+  SeqSpan* seqs;      // [B]
+  unsigned* status;   // [num_ctas]
+  uint8_t* qimg;      // [num_ctas] staged query images, qimg_stride bytes apart
+  int64_t qimg_stride;
   WsHeader* hdr;
-  int max_units;
   int num_ctas;
 };
 
-__device__ __forceinline__ void report(WsHeader* hdr, mla_status_t code) {
-  atomicCAS(&hdr->status, 0u, (unsigned)code);
+// The CTA of a split plan that holds block x, when `total` blocks are cut into n ranges
+// [c * total / n, (c + 1) * total / n): the largest c whose range starts at or before x.
+__host__ __device__ __forceinline__ int64_t range_lo(int64_t c, int64_t total, int64_t n) {
+  return c * total / n;
+}
+__host__ __device__ __forceinline__ int64_t range_of(int64_t x, int64_t total, int64_t n) {
+  return ((x + 1) * n + total - 1) / total - 1;
 }
 
 // Launchers (each returns the CUDA error of its launch).
-cudaError_t launch_plan(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
-                                    uint16_t* out, float* lse, cudaStream_t s);
-cudaError_t launch_reset_status(WsHeader* hdr, cudaStream_t s);
+                                    uint16_t* out, float* lse, int num_sms, cudaStream_t s);
 
 }  // namespace mla

@@ -1,0 +1,222 @@
+// mla_merge.cu -- the log-sum-exp merge of split-KV partial results.
+//
+// Per query row, lse = ln sum_s exp(lse_s) and out = sum_s exp(lse_s - lse) out_s, the
+// "merge by normalisation statistics" of position-sharded attention ("Scaling Kimi K3 on
+// AMD Instinct MI355X", section "缓存可复用，还要能一致地恢复").
+//
+// Where the partials come from: the attention kernel cuts the 128-key blocks of all
+// sequences, laid end to end, into one contiguous range per CTA; a sequence is split only
+// where a range boundary falls inside it, so its pieces sit on consecutive CTAs, and only
+// the first and the last unit of a CTA's range can hold part of a sequence. Partial slot 2c
+// is the piece that begins CTA c's range, slot 2c + 1 the piece that ends it (when the
+// range starts in an earlier sequence).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kMergeWarps = 8;
+constexpr int kMergeThreads = 32 * kMergeWarps;
+
+// Merge one dv chunk (32 * VEC values; lane l owns VEC consecutive ones) of one row from
+// `count` partials; slot_of(i) gives the partial index of piece i, whose row sits at
+// po[(slot * R + r) * 512] and pl[slot * R + r]. Latency, not bandwidth, sets the cost, so
+// the dependent rounds of loads are kept to two: every warp reduces the lse values itself
+// (no barrier), then warp w loads pieces w, w + 8, ... all at once and the warps' sums meet
+// in shared memory.
+template <int VEC, typename SlotOf>
+__device__ void merge_row_chunk(const float* __restrict__ po, const float* __restrict__ pl,
+                                int count, SlotOf slot_of, int64_t r, int64_t R, int chunk,
+                                uint16_t* __restrict__ out_row, float* lse_out) {
+  constexpr int W = 32 * VEC;  // dv per CTA
+  // pieces per batch and warp: enough that one batch covers the usual piece counts (a
+  // whole-GPU split of one sequence for VEC = 1), all loads in flight together
+  constexpr int NB = VEC >= 16 ? 2 : (VEC >= 4 ? 8 : 24);
+  constexpr int kLse = 8;  // lse values each lane keeps in registers (256 pieces)
+  __shared__ __align__(16) float s_acc[kMergeWarps][W];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (count <= 0) {  // nothing to merge: out = 0, lse = -inf
+    for (int x = threadIdx.x; x < W; x += kMergeThreads) out_row[chunk * W + x] = 0;
+    if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
+    return;
+  }
+  // lse = max + ln sum exp(lse_i - max), from one round of loads (a second, online pass
+  // only past 256 pieces)
+  // every load address is formed first (indices past the end clamped to the last piece)
+  // and every load issued before any is used, so that they travel together
+  float lv[kLse];
+  {
+    int64_t at[kLse];
+#pragma unroll
+    for (int j = 0; j < kLse; ++j) at[j] = slot_of(min(lane + 32 * j, count - 1)) * R + r;
+#pragma unroll
+    for (int j = 0; j < kLse; ++j) lv[j] = __ldg(pl + at[j]);
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kLse; ++j) {
+    if (lane + 32 * j >= count) lv[j] = -INFINITY;
+    m = fmaxf(m, lv[j]);
+  }
+  float sum = 0.f;
+  for (int i = lane + 32 * kLse; i < count; i += 32) {
+    const float x = __ldg(pl + slot_of(i) * R + r);
+    if (x > m) {
+      sum = sum * expf(m - x);
+      m = x;
+    }
+    sum += expf(x - m);
+  }
+  float mw = m;
+  for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+  sum = (m == -INFINITY) ? 0.f : sum * expf(m - mw);
+#pragma unroll
+  for (int j = 0; j < kLse; ++j)
+    if (lv[j] != -INFINITY) sum += expf(lv[j] - mw);
+  m = mw;
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  if (m != -INFINITY) {
+    for (int i0 = warp; i0 < count; i0 += NB * kMergeWarps) {
+      float v[NB][VEC];
+      float w[NB];
+      int64_t at[NB];
+#pragma unroll
+      for (int k = 0; k < NB; ++k) at[k] = slot_of(min(i0 + k * kMergeWarps, count - 1)) * R + r;
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        w[k] = __ldg(pl + at[k]);
+        const float* src = po + at[k] * kDV + chunk * W + lane * VEC;
+        if constexpr (VEC % 4 == 0) {
+#pragma unroll
+          for (int e = 0; e < VEC; e += 4) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(src + e));
+            v[k][e] = t.x;
+            v[k][e + 1] = t.y;
+            v[k][e + 2] = t.z;
+            v[k][e + 3] = t.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) v[k][e] = __ldg(src + e);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NB; ++k)
+        if (i0 + k * kMergeWarps >= count) w[k] = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        // an empty partial (lse = -inf) has weight 0; whatever its data holds is skipped
+        if (w[k] == -INFINITY) continue;
+        const float wk = expf(w[k] - lse);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] += wk * v[k][e];
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) s_acc[warp][lane * VEC + e] = acc[e];
+  __syncthreads();
+  // every thread finishes W / kMergeThreads (or one) of the chunk's outputs
+  for (int x = threadIdx.x; x < W; x += kMergeThreads) {
+    float t = 0.f;
+#pragma unroll
+    for (int g = 0; g < kMergeWarps; ++g) t += s_acc[g][x];
+    out_row[chunk * W + x] = __bfloat16_as_ushort(__float2bfloat16_rn(t));
+  }
+  if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = lse;
+}
+
+// Rows of the decode/verify path whose sequence was split over several CTAs, and rows of
+// sequences with no key at all (out = 0, lse = -inf). Launched as a programmatic dependent
+// of the attention kernel, whose grid it waits for.
+template <int VEC>
+__global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t row = blockIdx.x;  // b * R + r
+  const int chunk = blockIdx.y;
+  const int b = (int)(row / p.R);
+  const int64_t r = row % p.R;
+  const SeqSpan sp = p.seqs[b];
+  const int64_t total = p.hdr->total_blocks, n = p.num_ctas;
+  uint16_t* out_row = p.out + row * kDV;
+  float* lse_out = p.lse ? p.lse + row : nullptr;
+  if (sp.num_blocks == 0) {
+    for (int x = threadIdx.x; x < 32 * VEC; x += kMergeThreads) out_row[chunk * 32 * VEC + x] = 0;
+    if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
+    return;
+  }
+  const int64_t pre = sp.first_block;
+  // pieces: one per CTA range the sequence's blocks overlap (with fewer blocks than CTAs
+  // every range holds at most one block)
+  const int64_t c0 = range_of(pre, total, n);
+  const int count = (total >= n) ? (int)(range_of(pre + sp.num_blocks - 1, total, n) - c0 + 1)
+                                 : sp.num_blocks;
+  if (count == 1) return;  // the attention kernel wrote this row itself
+  // piece 0 takes the second slot of its CTA when that CTA's range began in an earlier
+  // sequence; every later piece begins its CTA's range
+  const int64_t first_odd = (range_lo(c0, total, n) < pre) ? 1 : 0;
+  auto slot_of = [&](int i) -> int64_t {
+    if (i == 0) return 2 * c0 + first_odd;
+    return 2 * ((total >= n) ? c0 + i : range_of(pre + i, total, n));
+  };
+  merge_row_chunk<VEC>(p.part_out, p.part_lse, count, slot_of, r, p.R, chunk, out_row, lse_out);
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_standalone_kernel(const float* po, const float* pl, int S, int64_t R, uint16_t* out,
+                            float* lse) {
+  const int64_t row = blockIdx.x;
+  merge_row_chunk<VEC>(po, pl, S, [](int i) -> int64_t { return i; }, row, R, blockIdx.y,
+                       out + row * kDV, lse ? lse + row : nullptr);
+}
+
+// Chunk width: whole 512-wide rows when there are rows enough to fill the GPU, narrower
+// chunks (more CTAs per row) for the few rows of a long history split over every SM.
+int merge_vec(int64_t rows, int num_sms) {
+  if (rows >= num_sms) return 16;
+  if (rows * 4 >= num_sms) return 4;
+  return 1;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.R;
+  const int vec = merge_vec(rows, p.num_ctas);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows, kDV / (32 * vec));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16>, p);
+  if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4>, p);
+  return cudaLaunchKernelEx(&cfg, merge_split_kernel<1>, p);
+}
+
+cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
+                                    uint16_t* out, float* lse, int num_sms, cudaStream_t s) {
+  const int vec = merge_vec(R, num_sms);
+  const dim3 grid((unsigned)R, kDV / (32 * vec));
+  if (vec == 16)
+    merge_standalone_kernel<16><<<grid, kMergeThreads, 0, s>>>(part_out, part_lse, S, R, out, lse);
+  else if (vec == 4)
+    merge_standalone_kernel<4><<<grid, kMergeThreads, 0, s>>>(part_out, part_lse, S, R, out, lse);
+  else
+    merge_standalone_kernel<1><<<grid, kMergeThreads, 0, s>>>(part_out, part_lse, S, R, out, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -233,6 +233,21 @@ def test_merge_lse_standalone():
     compare(out, lse, ref_out, ref_lse, "merge")
 
 
+def test_merge_lse_many_partials():
+    """More partials per row than the merge keeps in registers (256), few rows (narrow
+    chunks), and rows whose partials are all empty."""
+    g = torch.Generator().manual_seed(33)
+    S, R = 300, 3
+    po = torch.randn(S, R, 512, generator=g)
+    pl = torch.randn(S, R, generator=g) * 4
+    pl[::7, 0] = -math.inf
+    pl[:, 2] = -math.inf
+    out, lse = mla.mla_merge_lse(po.to(DEV), pl.to(DEV))
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.merge_lse(po.double().numpy(), pl.double().numpy())
+    compare(out, lse, ref_out, ref_lse, "merge, 300 partials")
+
+
 def test_cuda_graph_replay_matches_eager():
     inp = W.make_inputs("graph", [4000, 2500, 100], H=12, n_q=1, seed=32)
     kv = mla.KVCache.from_inputs(inp, DEV)
