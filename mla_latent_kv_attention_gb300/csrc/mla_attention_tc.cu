@@ -91,10 +91,11 @@ struct Misc {
   uint64_t q0_done;     // the first unit's query rows are staged (by warps 2-11 together)
   uint64_t q1_done;     // the second unit's rows are in this CTA's global query image
   uint64_t wg_bar[2];  // bounded barriers of the two softmax warpgroups (128 arrivals)
-  // decode/verify split plan of this CTA: blocks [x0, x1) of all sequences end to end;
-  // the range begins in sequence b0, whose first block is pre0
+  // decode/verify split plan of this CTA: positions [x0, x1) of the cost axis (all
+  // sequences end to end, each as kUnitCost fixed units then its blocks); its first unit
+  // is sequence b0 (length L0), whose first block sits at pre0
   long long plan_x0, plan_x1, plan_pre0;
-  int plan_b0, plan_L0;  // ... and b0's length
+  int plan_b0, plan_L0;
   int scan[kThreads / 32];
   uint32_t tmem_base;
   int abort;
@@ -131,8 +132,9 @@ struct UnitInfo {
   int slot;       // partial slot (when final_out == 0)
 };
 
-// Position in this CTA's list of units. Decode/verify: the sequences that overlap the CTA's
-// block range, in order (b, its first block pre, its length L). Prefill: unit index u.
+// Position in this CTA's list of units. Decode/verify: the sequences whose blocks overlap
+// the CTA's range, in order (b, the cost-axis position pre of its first block, its length
+// L). Prefill: unit index u.
 struct Cursor {
   int u;
   int b;
@@ -175,6 +177,7 @@ __device__ __forceinline__ Cursor next_unit(const DecodeArgs& a, Cursor c) {
     ++c.b;
     c.L = (c.b < a.p.B) ? seq_len_of(a.p, c.b) : 0;
   } while (c.b < a.p.B && c.L == 0);
+  c.pre += kUnitCost;  // the next sequence's fixed cost precedes its blocks
   return c;
 }
 
@@ -192,7 +195,8 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, const Misc* m
     x.j0 = 0;
     x.rows = a.rows;
     x.final_out = (blo == c.pre && bhi == c.pre + nb);
-    x.slot = 2 * (int)blockIdx.x + (blo == ms->plan_x0 ? 0 : 1);
+    // the CTA's first unit (nothing of an earlier sequence in its range) takes slot 2c
+    x.slot = 2 * (int)blockIdx.x + (c.pre - kUnitCost <= ms->plan_x0 ? 0 : 1);
   } else {
     // the last positions see the most keys: hand those out first
     const int pos0 = (a.num_units - 1 - c.u) * a.P;
@@ -429,13 +433,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;");
 
   if (!args.prefill) {
-    // ---- split plan (decode/verify), computed by every CTA for itself. The 128-key blocks
-    // of all sequences, laid end to end, are cut into gridDim.x nearly equal contiguous
-    // ranges; this CTA owns [x0, x1), one unit per sequence the range overlaps. A long
-    // history thus spreads over every SM ("Scaling Kimi K3 on AMD Instinct MI355X", section
+    // ---- split plan (decode/verify), computed by every CTA for itself. All sequences,
+    // laid end to end on a cost axis (each as kUnitCost fixed units, then its 128-key
+    // blocks), are cut into gridDim.x nearly equal contiguous ranges; this CTA owns
+    // [x0, x1), one unit per sequence whose blocks the range overlaps. A long history thus
+    // spreads over every SM ("Scaling Kimi K3 on AMD Instinct MI355X", section
     // "并行度必须适配真正的形状": hand the long history to more work groups), a batch of
-    // short sequences stays one unit per sequence, and a sequence is split only where a
-    // range boundary falls inside it.
+    // short sequences stays one unit per sequence, a sequence is split only where a range
+    // boundary falls inside it, and a CTA that crosses into another sequence takes fewer
+    // blocks.
     const int B = p.B, tid = threadIdx.x;
     const int per = (B + kThreads - 1) / kThreads;  // sequences per thread, contiguous
     const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
@@ -444,7 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int L = p.seq_lens[b];
       const int64_t cap = p.pt_stride * (int64_t)p.page_size;
       if (L < 0 || (int64_t)L > cap) report(ms, MLA_ERR_BOUNDS);
-      mine += blocks_of(seq_len_of(p, b));
+      const int nb = blocks_of(seq_len_of(p, b));
+      mine += nb > 0 ? nb + kUnitCost : 0;
     }
     // exclusive prefix of the per-thread block counts over the CTA
     long long incl = mine;
@@ -467,18 +474,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long x1 = total > 0 ? range_lo(c + 1, total, n) : 0;
     for (int b = b_lo; b < b_hi; ++b) {
       const int nb = blocks_of(seq_len_of(p, b));
-      if (nb > 0 && pre <= x0 && x0 < pre + nb && x0 < x1) {
+      const long long first = pre + kUnitCost;  // the sequence's first block
+      // the range's first unit: the sequence whose span holds x0, if the range reaches
+      // one of its blocks
+      if (nb > 0 && pre <= x0 && x0 < first + nb && first < x1 && x0 < x1) {
         ms->plan_b0 = b;
-        ms->plan_pre0 = pre;
+        ms->plan_pre0 = first;
         ms->plan_L0 = seq_len_of(p, b);
       }
-      if (b % (int)n == (int)c) p.seqs[b] = SeqSpan{(int)pre, nb};
-      pre += nb;
+      if (b % (int)n == (int)c) p.seqs[b] = SeqSpan{(int)first, nb};
+      if (nb > 0) pre = first + nb;
     }
     if (tid == 0) {
       ms->plan_x0 = x0;
       ms->plan_x1 = x1;
-      if (c == 0) p.hdr->total_blocks = (int)total;
+      if (c == 0) p.hdr->total_cost = (int)total;
     }
     __syncthreads();
     // Ask L2 for the first unit's query rows and page-table entries before the first TMA
@@ -496,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < qlines && has_unit(args, ms, c1))
         prefetch_l2(reinterpret_cast<const uint8_t*>(
                         p.q + ((int64_t)c1.b * p.R + ms->row_off[t / 9]) * kD) + (t % 9) * 128);
-      const int64_t pg0 = (ms->plan_x0 - ms->plan_pre0) * kKeyBlock / p.page_size;
+      const int64_t pg0 = max(0ll, ms->plan_x0 - ms->plan_pre0) * kKeyBlock / p.page_size;
       const int64_t pg = pg0 + (int64_t)(t - 304) * 32;  // four lines of 32 entries
       if (t >= 304 && t < 304 + 4 && pg < p.pt_stride)
         prefetch_l2(p.page_table + (int64_t)b0 * p.pt_stride + pg);

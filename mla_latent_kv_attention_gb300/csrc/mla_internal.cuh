@@ -11,16 +11,23 @@ namespace mla {
 constexpr int kD = MLA_D;
 constexpr int kDV = MLA_DV;
 constexpr int kKeyBlock = 128;     // keys per work block: the unit of split planning
+// Split planning charges every sequence this many blocks' worth of time on top of its own
+// blocks: a unit's epilogue and the refill of the pipeline after it. A CTA that takes a
+// unit boundary gets correspondingly fewer blocks.
+constexpr int kUnitCost = 5;
 constexpr int kMaxRows = MLA_MAX_HEADS * MLA_MAX_NQ;  // query rows per sequence (64)
 
 // Workspace header at offset 0 (256 bytes).
 struct WsHeader {
   int num_ctas;      // CTAs of the last attention launch: status slots [0, num_ctas) are its
-  int total_blocks;  // decode/verify: 128-key blocks of all sequences, end to end
+  int total_cost;    // decode/verify: length of the plan's cost axis (see SeqSpan)
   int pad[62];
 };
 
-// A sequence's 128-key blocks in the flat block order of all sequences laid end to end.
+// A sequence's place on the split plan's cost axis: all sequences laid end to end, each as
+// kUnitCost units of fixed cost followed by its 128-key blocks (an empty sequence takes no
+// room). first_block is the position of its first block; CTA c owns the positions
+// [c * total_cost / n, (c + 1) * total_cost / n).
 struct SeqSpan {
   int first_block, num_blocks;
 };

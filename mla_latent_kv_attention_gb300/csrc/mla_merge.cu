@@ -4,12 +4,12 @@
 // "merge by normalisation statistics" of position-sharded attention ("Scaling Kimi K3 on
 // AMD Instinct MI355X", section "缓存可复用，还要能一致地恢复").
 //
-// Where the partials come from: the attention kernel cuts the 128-key blocks of all
-// sequences, laid end to end, into one contiguous range per CTA; a sequence is split only
-// where a range boundary falls inside it, so its pieces sit on consecutive CTAs, and only
-// the first and the last unit of a CTA's range can hold part of a sequence. Partial slot 2c
-// is the piece that begins CTA c's range, slot 2c + 1 the piece that ends it (when the
-// range starts in an earlier sequence).
+// Where the partials come from: the attention kernel lays all sequences end to end on a
+// cost axis (a fixed cost per sequence, then its 128-key blocks) and cuts it into one
+// contiguous range per CTA; a sequence is split only where a range boundary falls inside
+// its blocks, so its pieces sit on consecutive CTAs, and only the first and the last unit
+// of a CTA's range can hold part of a sequence. Partial slot 2c is the piece that is CTA
+// c's first unit, slot 2c + 1 the piece that ends its range after an earlier sequence.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p
   const int b = (int)(row / p.R);
   const int64_t r = row % p.R;
   const SeqSpan sp = p.seqs[b];
-  const int64_t total = p.hdr->total_blocks, n = p.num_ctas;
+  const int64_t total = p.hdr->total_cost, n = p.num_ctas;
   uint16_t* out_row = p.out + row * kDV;
   float* lse_out = p.lse ? p.lse + row : nullptr;
   if (sp.num_blocks == 0) {
@@ -160,9 +160,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p
   const int count = (total >= n) ? (int)(range_of(pre + sp.num_blocks - 1, total, n) - c0 + 1)
                                  : sp.num_blocks;
   if (count == 1) return;  // the attention kernel wrote this row itself
-  // piece 0 takes the second slot of its CTA when that CTA's range began in an earlier
-  // sequence; every later piece begins its CTA's range
-  const int64_t first_odd = (range_lo(c0, total, n) < pre) ? 1 : 0;
+  // piece 0 takes the second slot of its CTA when that CTA's range began before this
+  // sequence's span (in an earlier sequence); every later piece begins its CTA's range
+  const int64_t first_odd = (range_lo(c0, total, n) < pre - kUnitCost) ? 1 : 0;
   auto slot_of = [&](int i) -> int64_t {
     if (i == 0) return 2 * c0 + first_odd;
     return 2 * ((total >= n) ? c0 + i : range_of(pre + i, total, n));
