@@ -24,19 +24,18 @@ constexpr int kMergeThreads = 32 * kMergeWarps;
 
 // Merge one dv chunk (32 * VEC values; lane l owns VEC consecutive ones) of one row from
 // `count` partials; slot_of(i) gives the partial index of piece i, whose row sits at
-// po[(slot * R + r) * 512] and pl[slot * R + r]. Latency, not bandwidth, sets the cost, so
-// the dependent rounds of loads are kept to two: every warp reduces the lse values itself
-// (no barrier), then warp w loads pieces w, w + 8, ... all at once and the warps' sums meet
-// in shared memory.
+// po[(slot * R + r) * 512] and pl[slot * R + r]. Latency sets the cost (the partials were
+// written by the kernel just before), so everything is loaded in one round: each lane the
+// lse values it reduces (every warp reduces them all, no barrier) and warp w's pieces
+// w, w + 8, ..., with their own lse values for the weights; only pieces past the first
+// batch, or lse values past 256, take further rounds. The warps' sums meet in shared memory.
 template <int VEC, typename SlotOf>
 __device__ void merge_row_chunk(const float* __restrict__ po, const float* __restrict__ pl,
                                 int count, SlotOf slot_of, int64_t r, int64_t R, int chunk,
                                 uint16_t* __restrict__ out_row, float* lse_out) {
-  constexpr int W = 32 * VEC;  // dv per CTA
-  // pieces per batch and warp: enough that one batch covers the usual piece counts (a
-  // whole-GPU split of one sequence for VEC = 1), all loads in flight together
-  constexpr int NB = VEC >= 16 ? 2 : (VEC >= 4 ? 8 : 24);
-  constexpr int kLse = 8;  // lse values each lane keeps in registers (256 pieces)
+  constexpr int W = 32 * VEC;                             // dv per CTA
+  constexpr int NB = VEC >= 16 ? 2 : (VEC >= 4 ? 8 : 24);  // pieces per batch and warp
+  constexpr int kLse = 8;                                 // lse values per lane (256 pieces)
   __shared__ __align__(16) float s_acc[kMergeWarps][W];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (count <= 0) {  // nothing to merge: out = 0, lse = -inf
@@ -44,10 +43,37 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
     if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
     return;
   }
-  // lse = max + ln sum exp(lse_i - max), from one round of loads (a second, online pass
-  // only past 256 pieces)
-  // every load address is formed first (indices past the end clamped to the last piece)
-  // and every load issued before any is used, so that they travel together
+  // load the pieces i0 + k * 8 (k < NB) of this warp: weights' lse values and data;
+  // indices past the end are clamped to the last piece (a valid address) and dropped later
+  float v[NB][VEC];
+  float w[NB];
+  auto load_batch = [&](int i0) {
+    int64_t at[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) at[k] = slot_of(min(i0 + k * kMergeWarps, count - 1)) * R + r;
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      w[k] = __ldg(pl + at[k]);
+      const float* src = po + at[k] * kDV + chunk * W + lane * VEC;
+      if constexpr (VEC % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4) {
+          const float4 t = __ldg(reinterpret_cast<const float4*>(src + e));
+          v[k][e] = t.x;
+          v[k][e + 1] = t.y;
+          v[k][e + 2] = t.z;
+          v[k][e + 3] = t.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v[k][e] = __ldg(src + e);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k)
+      if (i0 + k * kMergeWarps >= count) w[k] = -INFINITY;
+  };
+  // round one: this lane's share of the lse values, and the warp's first batch
   float lv[kLse];
   {
     int64_t at[kLse];
@@ -56,6 +82,8 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
 #pragma unroll
     for (int j = 0; j < kLse; ++j) lv[j] = __ldg(pl + at[j]);
   }
+  load_batch(warp);
+  // lse = max + ln sum exp(lse_i - max)
   float m = -INFINITY;
 #pragma unroll
   for (int j = 0; j < kLse; ++j) {
@@ -63,7 +91,7 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
     m = fmaxf(m, lv[j]);
   }
   float sum = 0.f;
-  for (int i = lane + 32 * kLse; i < count; i += 32) {
+  for (int i = lane + 32 * kLse; i < count; i += 32) {  // online, past 256 pieces
     const float x = __ldg(pl + slot_of(i) * R + r);
     if (x > m) {
       sum = sum * expf(m - x);
@@ -84,33 +112,7 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   if (m != -INFINITY) {
-    for (int i0 = warp; i0 < count; i0 += NB * kMergeWarps) {
-      float v[NB][VEC];
-      float w[NB];
-      int64_t at[NB];
-#pragma unroll
-      for (int k = 0; k < NB; ++k) at[k] = slot_of(min(i0 + k * kMergeWarps, count - 1)) * R + r;
-#pragma unroll
-      for (int k = 0; k < NB; ++k) {
-        w[k] = __ldg(pl + at[k]);
-        const float* src = po + at[k] * kDV + chunk * W + lane * VEC;
-        if constexpr (VEC % 4 == 0) {
-#pragma unroll
-          for (int e = 0; e < VEC; e += 4) {
-            const float4 t = __ldg(reinterpret_cast<const float4*>(src + e));
-            v[k][e] = t.x;
-            v[k][e + 1] = t.y;
-            v[k][e + 2] = t.z;
-            v[k][e + 3] = t.w;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) v[k][e] = __ldg(src + e);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < NB; ++k)
-        if (i0 + k * kMergeWarps >= count) w[k] = -INFINITY;
+    for (int i0 = warp;;) {
 #pragma unroll
       for (int k = 0; k < NB; ++k) {
         // an empty partial (lse = -inf) has weight 0; whatever its data holds is skipped
@@ -119,6 +121,9 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[e] += wk * v[k][e];
       }
+      i0 += NB * kMergeWarps;
+      if (i0 >= count) break;
+      load_batch(i0);
     }
   }
 #pragma unroll
