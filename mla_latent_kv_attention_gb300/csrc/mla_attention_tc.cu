@@ -81,6 +81,7 @@ struct Misc {
   alignas(16) float red[2][48 * 4];  // per-tile warp maxima, [row][warp]
   alignas(16) float lred[4][48];
   alignas(16) float alpha[4][48];    // per-warp copy of this tile's rescale factors
+  alignas(16) int grow[2][8];        // per tile parity and warp: some row's max moves
   alignas(16) int row_j[48];         // new-position index j of each row (very negative for padding)
   alignas(16) int row_off[48];       // j * H + h: the row's index among its sequence's rows
   alignas(8) uint64_t kv_full[kStages], kv_empty[kStages];
@@ -102,7 +103,8 @@ struct Misc {
   unsigned status;  // this CTA's first error
 };
 static_assert(offsetof(Misc, row_scale) % 16 == 0 && offsetof(Misc, red) % 16 == 0 &&
-                  offsetof(Misc, lred) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0,
+                  offsetof(Misc, lred) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0 &&
+                  offsetof(Misc, grow) % 16 == 0,
               "vector-accessed arrays must be 16-byte aligned");
 static_assert(offsetof(Misc, kv_full) % 8 == 0, "mbarriers must be 8-byte aligned");
 
@@ -811,30 +813,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kabs > lim) x[r] = -INFINITY;
           }
         }
-        // tile max per row: warp max in hardware, then the four warps through shared memory
-        float* red = &ms->red[tile & 1][0];
+        // The running max of a row moves only when some score exceeds it by more than the
+        // 2^8 headroom (kRescaleGap in log2 units); only then is the exact tile max needed.
+        // The warps of the warpgroup first agree whether that happens anywhere, and the
+        // common case skips the exchange of per-row maxima.
+        bool over = false;
 #pragma unroll
-        for (int r = 0; r < RH; ++r) {
-          const float v = warp_max(x[r]);
-          if (lane == 0) red[(rb + r) * 4 + wq] = v;
-        }
+        for (int r = 0; r < RH; ++r) over |= (x[r] > m[r] + kRescaleGap);
+        over = __any_sync(0xffffffffu, over);
+        if (lane == 0) ms->grow[tile & 1][wg * 4 + wq] = over ? 1 : 0;
         if (!(ok = wg_sync())) break;
+        const int4 gf = *reinterpret_cast<const int4*>(&ms->grow[tile & 1][wg * 4]);
         bool need_rescale = false;
         float moff[RH];
+        if ((gf.x | gf.y | gf.z | gf.w) != 0) {
+          // tile max per row: warp max in hardware, then the four warps through shared memory
+          float* red = &ms->red[tile & 1][0];
 #pragma unroll
-        for (int r = 0; r < RH; ++r) {
-          const float4 t4 = *reinterpret_cast<const float4*>(&red[(rb + r) * 4]);
-          const float tm = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
-          float al = 1.f;
-          if (tm > m[r] + kRescaleGap) {  // lazy: small increases are absorbed by the 2^8 headroom
-            al = ex2(m[r] - tm);  // 0 when m was -inf (nothing accumulated yet)
-            need_rescale |= (m[r] != -INFINITY);
-            l[r] *= al;
-            m[r] = tm;
+          for (int r = 0; r < RH; ++r) {
+            const float v = warp_max(x[r]);
+            if (lane == 0) red[(rb + r) * 4 + wq] = v;
           }
-          if (lane == 0) ms->alpha[wq][rb + r] = al;
-          moff[r] = (m[r] == -INFINITY) ? 0.f : m[r] - kPScale;
+          if (!(ok = wg_sync())) break;
+#pragma unroll
+          for (int r = 0; r < RH; ++r) {
+            const float4 t4 = *reinterpret_cast<const float4*>(&red[(rb + r) * 4]);
+            const float tm = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
+            float al = 1.f;
+            if (tm > m[r] + kRescaleGap) {  // lazy: small increases are absorbed by the headroom
+              al = ex2(m[r] - tm);  // 0 when m was -inf (nothing accumulated yet)
+              need_rescale |= (m[r] != -INFINITY);
+              l[r] *= al;
+              m[r] = tm;
+            }
+            if (lane == 0) ms->alpha[wq][rb + r] = al;
+          }
         }
+#pragma unroll
+        for (int r = 0; r < RH; ++r) moff[r] = (m[r] == -INFINITY) ? 0.f : m[r] - kPScale;
         // p = 2^(x - m + 4) <= 2^8 rounded to fp16, carried exactly by three e4m3 terms
         uint32_t w1[RH / 4], w2[RH / 4], w3[RH / 4];
 #pragma unroll
