@@ -54,12 +54,21 @@ constexpr int kPrefetchTiles = 1;    // tiles the producer pulls into L2 ahead o
 template <int RP>
 struct Cfg {
   static constexpr int NQK = 2 * RP;                    // two query terms per row
-  static constexpr bool kStackP = RP <= 32;
-  static constexpr int OCOLS = kStackP ? 3 * RP : RP;   // O^T columns per dv chunk
-  static constexpr int NPV = OCOLS;
-  static constexpr int kSCol = 0;                       // S^T buffers: [0, 2 NQK)
-  static constexpr int kOCol = 2 * NQK;                 // O^T: 4 chunks of OCOLS
-  static constexpr int kTmemUsed = 2 * NQK + 4 * OCOLS;
+  // S^T buffers: two (the next tile's scores land while the softmax works on this one),
+  // one at 48 rows, where TMEM is needed for stacked O chunks
+  static constexpr int kSBuf = (RP == 48) ? 1 : 2;
+  // O^T chunk c (128 dv lanes) holds the three P terms' products side by side ("stacked":
+  // one N = 3 RP MMA per k-step, the V^T tile read once) or summed in one accumulator
+  // (three N = RP MMAs per k-step, V^T read three times). Stacked everywhere up to 32
+  // rows; at 48 rows TMEM holds two stacked chunks and two summed ones.
+  static constexpr int kStackedChunks = (RP == 48) ? 2 : 4;
+  static constexpr __host__ __device__ int oterms(int c) { return c < kStackedChunks ? 3 : 1; }
+  static constexpr int kSCol = 0;                       // S^T buffers: [0, kSBuf NQK)
+  static constexpr int kOCol = kSBuf * NQK;             // O^T chunks from here
+  static constexpr __host__ __device__ int ocol(int c) {
+    return kOCol + (c < kStackedChunks ? c * 3 * RP : kStackedChunks * 3 * RP + (c - kStackedChunks) * RP);
+  }
+  static constexpr int kTmemUsed = ocol(3) + oterms(3) * RP;
   static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static constexpr int kQBytes = NQK * kD;
   // query operand buffers: two (the next unit is staged during this one) when they fit
@@ -634,9 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_or_abort(&ms->q_full[qslot], (units_done / C::kQB) & 1, ms, p))) break;
         const uint32_t qoff = (uint32_t)(qslot * C::kQBytes) >> 4;
         for (int t = 0; t < n; ++t, ++g) {
-          const int s = g % kStages, sb = g & 1;
+          const int s = g % kStages, sb = g % C::kSBuf;
           if (!(ok = wait_or_abort(&ms->kv_full[s], (g / kStages) & 1, ms, p))) break;
-          if (!(ok = wait_or_abort(&ms->s_empty[sb], ((g >> 1) & 1) ^ 1, ms, p))) break;
+          if (!(ok = wait_or_abort(&ms->s_empty[sb], ((g / C::kSBuf) & 1) ^ 1, ms, p))) break;
           tc_fence_after();
           const uint32_t soff = (uint32_t)(s * kStageBytes) >> 4;
           const uint32_t d = tmem + C::kSCol + sb * C::NQK;
@@ -663,7 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // PV of every tile the moment its probabilities are in shared memory; completion hands
     // the KV stage back to the producer and lets the softmax reuse P and rescale O.
     if (lane == 0) {
-      constexpr uint32_t idesc_pv = instr_desc(0, 0, 1, 1, 128, C::NPV);
+      constexpr uint32_t idesc_stacked = instr_desc(0, 0, 1, 1, 128, 3 * RP);
+      constexpr uint32_t idesc_term = instr_desc(0, 0, 1, 1, 128, RP);
       const uint64_t a0 = smem_desc(smem_addr(smem + C::kOffStages), kChunkBytes, 1024, Swizzle::k128B);
       const uint64_t b0 = smem_desc(smem_addr(pbuf), 128, 2048, Swizzle::kNone);
       uint32_t g = 0;
@@ -675,17 +685,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int s = g % kStages;
           const uint32_t soff = (uint32_t)(s * kStageBytes) >> 4;
-          // consecutive MMAs go to different dv chunks' accumulators
+          // consecutive MMAs go to different dv chunks' accumulators where they can
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-            for (int term = 0; term < (C::kStackP ? 1 : 3); ++term) {
+            for (int term = 0; term < 3; ++term) {
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
-                const uint32_t d = tmem + C::kOCol + c * C::OCOLS;
                 const uint64_t a = a0 + soff + ((c * kChunkBytes + ks * 4096) >> 4);
-                const uint64_t b = b0 + ((term * (RP / 16) * 2048 + ks * 512) >> 4);
-                mma_f8f6f4(d, a, b, idesc_pv, t > 0 || ks > 0 || term > 0);
+                if (C::oterms(c) == 3) {  // stacked: one MMA over all three terms' rows
+                  if (term == 0)
+                    mma_f8f6f4(tmem + C::ocol(c), a, b0 + ((ks * 512) >> 4), idesc_stacked,
+                               t > 0 || ks > 0);
+                } else {  // summed: one MMA per term into the same accumulator
+                  mma_f8f6f4(tmem + C::ocol(c), a, b0 + ((term * (RP / 16) * 2048 + ks * 512) >> 4),
+                             idesc_term, t > 0 || ks > 0 || term > 0);
+                }
               }
             }
           }
@@ -784,11 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         l[r] = 0.f;
       }
       for (int t = 0; t < ntiles; ++t, ++tile) {
-        const int sb = tile & 1;
+        const int sb = tile % C::kSBuf;
         const int s = tile % kStages;
         const int k0 = un.key_lo + t * kTileKeys;
         const int kabs = k0 + i;
-        if (!(ok = wait_or_abort(&ms->s_full[sb], (tile >> 1) & 1, ms, p))) break;
+        if (!(ok = wait_or_abort(&ms->s_full[sb], (tile / C::kSBuf) & 1, ms, p))) break;
         tc_fence_after();
         float x[RH];
         {
@@ -887,10 +902,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
-              for (int term = 0; term < (C::kStackP ? 3 : 1); ++term) {
+              for (int term = 0; term < C::oterms(c); ++term) {
 #pragma unroll
                 for (int cc = 0; cc < RH; cc += 8) {
-                  const uint32_t a = tmem + lane_addr + C::kOCol + c * C::OCOLS + term * RP + rb + cc;
+                  const uint32_t a = tmem + lane_addr + C::ocol(c) + term * RP + rb + cc;
                   float v[8];
                   tmem_ld8(a, v);
                   tmem_wait_ld();
@@ -950,14 +965,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        constexpr int NT = C::kStackP ? 3 : 1;
-        float o[NT][RH];
+        const int NT = C::oterms(c);
+        float o[3][RH];
 #pragma unroll
-        for (int term = 0; term < NT; ++term)
+        for (int term = 0; term < 3; ++term)
 #pragma unroll
           for (int cc = 0; cc < RH; cc += 8) {
+            if (term >= NT) break;
             float v[8];
-            tmem_ld8(tmem + lane_addr + C::kOCol + c * C::OCOLS + term * RP + rb + cc, v);
+            tmem_ld8(tmem + lane_addr + C::ocol(c) + term * RP + rb + cc, v);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[term][cc + e] = v[e];
           }
@@ -967,7 +983,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rb + r >= R) break;
           float acc = o[0][r];
 #pragma unroll
-          for (int term = 1; term < NT; ++term) acc += o[term][r];
+          for (int term = 1; term < 3; ++term)
+            if (term < NT) acc += o[term][r];
           const int dv = c * 128 + i;
           const int roff = ms->row_off[rb + r];
           if (final_out) {
