@@ -559,6 +559,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t rows64 = p.num_pages * (int64_t)p.page_size;
       const int total_rows = rows64 > 0x7fffff00 ? 0x7fffff00 : (int)rows64;
       uint32_t fill = 0;  // tiles issued so far
+      // Decode reads each cached row once per call: its lines should not push out of L2
+      // what is reused (code, query rows, page tables, the partials the merge reads next).
+      // Prefill re-reads the same rows for every unit and keeps the default policy.
+      const uint64_t read_once = args.prefill ? l2_policy_evict_normal() : l2_policy_evict_first();
       // L2 prefetch cursor: runs kPrefetchTiles tiles ahead of the TMA loads so that they
       // find their pages in L2 (deeper than the two shared-memory stages allow).
       Cursor pf_c = first_unit(args, ms);
@@ -611,8 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              tma_load_2d(st + c * kChunkBytes + h * 8192, &map_main, c * 128, y, &ms->kv_full[s]);
-            tma_load_2d(st + kTailOffset + h * 4096, &map_tail, 0, y, &ms->kv_full[s]);
+              tma_load_2d_hint(st + c * kChunkBytes + h * 8192, &map_main, c * 128, y,
+                               &ms->kv_full[s], read_once);
+            tma_load_2d_hint(st + kTailOffset + h * 4096, &map_tail, 0, y, &ms->kv_full[s], read_once);
           }
           ++fill;
           prefetch_upto(fill + kPrefetchTiles);
