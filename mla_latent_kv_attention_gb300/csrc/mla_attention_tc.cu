@@ -20,9 +20,10 @@
 // Softmax is online over key tiles; one warpgroup owns one key per thread (its TMEM
 // lane), so the running max per row needs a cross-warp reduction each tile.
 //
-// Roles (384 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the score MMAs,
-// warp 3 issues the value MMAs, warp 2 stages query rows, warps 4-11 (two warpgroups)
-// run the softmax and write the epilogue. Every wait is bounded.
+// Roles: warp 0 issues TMA, warp 1 owns TMEM and issues the score MMAs, warp 3 issues the
+// value MMAs, warp 2 stages query rows, and from warp 4 on two warpgroups (three with 48
+// rows per unit: 384 or 512 threads) run the softmax and write the epilogue. Every wait is
+// bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -43,7 +44,7 @@ constexpr int kStages = 2;
 constexpr int kChunkBytes = 16384;                     // 128 keys x 128 bytes, SW128
 constexpr int kTailOffset = 4 * kChunkBytes;            // 128 keys x 64 bytes, SW64
 constexpr int kStageBytes = kTailOffset + 2 * 4096;     // 73,728
-constexpr int kThreads = 384;  // producer, 2 MMA issuers, query stager, 2 softmax warpgroups
+constexpr int kMaxThreads = 512;  // producer, 2 MMA issuers, query stager, 2-3 softmax warpgroups
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s
 constexpr float kLog2e = 1.4426950408889634f;
@@ -53,6 +54,11 @@ constexpr int kPrefetchTiles = 1;    // tiles the producer pulls into L2 ahead o
 
 template <int RP>
 struct Cfg {
+  // softmax warpgroups: three at 48 rows (16 rows per thread), else two
+  static constexpr int kNWG = (RP == 48) ? 3 : 2;
+  static constexpr int kThreads = 128 + 128 * kNWG;
+  static constexpr int kRH = RP / kNWG;                // query rows per softmax thread
+  static constexpr int kStageWarps = kThreads / 32 - 2;  // warps 2.. stage the first units
   static constexpr int NQK = 2 * RP;                    // two query terms per row
   // S^T buffers: two (the next tile's scores land while the softmax works on this one),
   // one at 48 rows, where TMEM is needed for stacked O chunks
@@ -90,7 +96,7 @@ struct Misc {
   alignas(16) float red[2][48 * 4];  // per-tile warp maxima, [row][warp]
   alignas(16) float lred[4][48];
   alignas(16) float alpha[4][48];    // per-warp copy of this tile's rescale factors
-  alignas(16) int grow[2][8];        // per tile parity and warp: some row's max moves
+  alignas(16) int grow[2][12];       // per tile parity and warp: some row's max moves
   alignas(16) int row_j[48];         // new-position index j of each row (very negative for padding)
   alignas(16) int row_off[48];       // j * H + h: the row's index among its sequence's rows
   alignas(8) uint64_t kv_full[kStages], kv_empty[kStages];
@@ -98,15 +104,15 @@ struct Misc {
   uint64_t p_full, pv_done;
   uint64_t q_full[2];   // query operand buffer holds its unit's terms
   uint64_t q_empty[2];  // the unit that used the buffer has finished its scores
-  uint64_t q0_done;     // the first unit's query rows are staged (by warps 2-11 together)
+  uint64_t q0_done;     // the first unit's query rows are staged (by warps 2.. together)
   uint64_t q1_done;     // the second unit's rows are in this CTA's global query image
-  uint64_t wg_bar[2];  // bounded barriers of the two softmax warpgroups (128 arrivals)
+  uint64_t wg_bar[3];  // bounded barriers of the softmax warpgroups (128 arrivals)
   // decode/verify split plan of this CTA: positions [x0, x1) of the cost axis (all
   // sequences end to end, each as kUnitCost fixed units then its blocks); its first unit
   // is sequence b0 (length L0), whose first block sits at pre0
   long long plan_x0, plan_x1, plan_pre0;
   int plan_b0, plan_L0;
-  int scan[kThreads / 32];
+  int scan[kMaxThreads / 32];
   uint32_t tmem_base;
   int abort;
   unsigned status;  // this CTA's first error
@@ -387,7 +393,7 @@ __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int
 }
 
 template <int RP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ DecodeArgs args,
                      const __grid_constant__ CUtensorMap map_main,
                      const __grid_constant__ CUtensorMap map_tail) {
@@ -408,17 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->s_full[s], 1);
-      mbar_init(&ms->s_empty[s], 256);
-      mbar_init(&ms->wg_bar[s], 128);
+      mbar_init(&ms->s_empty[s], 128 * C::kNWG);
     }
-    mbar_init(&ms->p_full, 256);
+    for (int w = 0; w < C::kNWG; ++w) mbar_init(&ms->wg_bar[w], 128);
+    mbar_init(&ms->p_full, 128 * C::kNWG);
     mbar_init(&ms->pv_done, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->q_full[s], 1);
       mbar_init(&ms->q_empty[s], 1);
     }
-    mbar_init(&ms->q0_done, 320);
-    mbar_init(&ms->q1_done, 320);
+    mbar_init(&ms->q0_done, 32 * C::kStageWarps);
+    mbar_init(&ms->q1_done, 32 * C::kStageWarps);
     ms->abort = 0;
     ms->status = 0;
     ms->plan_b0 = args.p.B;  // no unit unless the plan finds one
@@ -454,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // boundary falls inside it, and a CTA that crosses into another sequence takes fewer
     // blocks.
     const int B = p.B, tid = threadIdx.x;
-    const int per = (B + kThreads - 1) / kThreads;  // sequences per thread, contiguous
+    const int per = (B + C::kThreads - 1) / C::kThreads;  // sequences per thread, contiguous
     const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
     long long mine = 0;
     for (int b = b_lo; b < b_hi; ++b) {
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     long long before = 0, total = 0;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < C::kThreads / 32; ++w) {
       if (w < warp) before += ms->scan[w];
       total += ms->scan[w];
     }
@@ -507,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // both are on the path to the first scores.
     if (warp >= 2 && ms->plan_b0 < B) {
       const int b0 = ms->plan_b0;
-      const int t = threadIdx.x - 64;  // 320 threads
+      const int t = threadIdx.x - 64;  // 320 threads or more
       const int qlines = args.rows * 9;  // 1,152 bytes per row
       if (t < qlines)
         prefetch_l2(reinterpret_cast<const uint8_t*>(
@@ -525,10 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
 
-  // The first unit's queries are on every CTA's critical path: warps 2-11 stage them into
+  // The first unit's queries are on every CTA's critical path: warps 2.. stage them into
   // shared memory together (about two rows each). Later units' rows go to this CTA's query
   // image in global memory and reach shared memory in one bulk copy when their unit starts
-  // (staging takes one warp far longer than a unit boundary may last): warps 2-11 stage the
+  // (staging takes one warp far longer than a unit boundary may last): warps 2.. stage the
   // second unit there before the first key tile lands, the stager warp each later one while
   // the unit before it runs.
   if (warp >= 2) {
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (has_unit(args, ms, c0)) {
       const UnitInfo ui = unit_info(args, ms, c0);
       stage_rows<RP>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, qbuf,
-                     ms->row_scale[0], warp - 2, 10, lane);
+                     ms->row_scale[0], warp - 2, C::kStageWarps, lane);
       fence_proxy_async_smem();
       mbar_arrive(&ms->q0_done);
       Cursor c1 = next_unit(args, c0);
@@ -546,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const UnitInfo u1 = unit_info(args, ms, c1);
         uint8_t* img = p.qimg + (int64_t)blockIdx.x * p.qimg_stride;
         stage_rows<RP>(p, u1.rows, ms->row_off, p.q + (int64_t)u1.qrow0 * kD, img,
-                       reinterpret_cast<float*>(img + C::kQBytes), warp - 2, 10, lane);
+                       reinterpret_cast<float*>(img + C::kQBytes), warp - 2, C::kStageWarps, lane);
         fence_proxy_async_global();
         mbar_arrive(&ms->q1_done);
       }
@@ -726,13 +732,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitInfo ui = unit_info(args, ms, cu);
       if (tiles_in(ui) == 0) continue;
       const int slot = k % C::kQB;
-      if (k == 0) {  // staged into shared memory by warps 2-11 in the prologue
+      if (k == 0) {  // staged into shared memory by warps 2.. in the prologue
         if (!wait_or_abort(&ms->q0_done, 0, ms, p)) break;
         if (lane == 0) mbar_arrive(&ms->q_full[0]);
         ++k;
         continue;
       }
-      if (k == 1) {  // staged into the image by warps 2-11 in the prologue
+      if (k == 1) {  // staged into the image by warps 2.. in the prologue
         if (!wait_or_abort(&ms->q1_done, 0, ms, p)) break;
       } else {
         // the image is free once the previous unit's copy out of it has landed
@@ -754,9 +760,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------------ softmax warpgroups
-    // Two warpgroups, each owning half of the query rows; thread i of a warpgroup owns key
-    // i of the tile (its TMEM lane).
-    constexpr int RH = RP / 2;
+    // Two or three warpgroups, each owning an equal share of the query rows; thread i of a
+    // warpgroup owns key i of the tile (its TMEM lane).
+    constexpr int RH = C::kRH;
     const int wg = (warp - kSoftmaxWarp0) >> 2;
     const int rb = wg * RH;  // rows [rb, rb + RH)
     const int wq = warp & 3;  // TMEM lane quadrant
@@ -1091,7 +1097,7 @@ cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensor
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Cfg<RP>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr;
