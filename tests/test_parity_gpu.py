@@ -81,6 +81,19 @@ def _sample_rows(B, n_q, H, extra, seed, must=()):
     return np.array(sorted(rows), dtype=np.int32)
 
 
+@pytest.mark.parametrize("n_q", [1, 4])
+def test_many_short_sequences(n_q):
+    """Hundreds of short sequences: every CTA's block range covers several sequences, so
+    units past a CTA's second go through the staged query image, and most sequences are
+    whole units written without a merge."""
+    g = np.random.default_rng(40 + n_q)
+    lens = [int(x) for x in g.integers(1, 400, size=500)]
+    lens[7] = 0
+    lens[300] = 0
+    inp = W.make_inputs("short", lens, H=12, n_q=n_q, seed=43 + n_q)
+    check_full(inp, f"500 short sequences, n_q={n_q}")
+
+
 def test_spec_verify_sampled():
     inp = W.spec_verify()
     out, lse = run_split(inp)
