@@ -81,6 +81,21 @@ def _sample_rows(B, n_q, H, extra, seed, must=()):
     return np.array(sorted(rows), dtype=np.int32)
 
 
+@pytest.mark.parametrize("page_size,n_q", [(128, 1), (256, 4), (128, 3)])
+def test_larger_pages(page_size, n_q):
+    """Pages of 128 and 256 positions: a 128-key tile is one page, or half of one."""
+    inp = W.make_inputs("pages", [3000, 129, 777, 4096], H=12, n_q=n_q, page_size=page_size,
+                        seed=page_size + n_q)
+    check_full(inp, f"page_size={page_size} n_q={n_q}")
+
+
+def test_causal_prefill_larger_pages():
+    inp = W.make_inputs("prefill_pages", [1300], H=12, n_q=300, page_size=256, seed=52)
+    out, lse = run_prefill(inp)
+    ref_out, ref_lse = oracle.attention(inp)
+    compare(out, lse, ref_out, ref_lse, "prefill, 256-position pages")
+
+
 @pytest.mark.parametrize("n_q", [1, 4])
 def test_many_short_sequences(n_q):
     """Hundreds of short sequences: every CTA's block range covers several sequences, so
