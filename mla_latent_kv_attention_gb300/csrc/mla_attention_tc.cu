@@ -42,8 +42,7 @@ using namespace sm100;
 constexpr int kTileKeys = 128;
 constexpr int kStages = 2;
 constexpr int kChunkBytes = 16384;                     // 128 keys x 128 bytes, SW128
-constexpr int kTailOffset = 4 * kChunkBytes;            // 128 keys x 64 bytes, SW64
-constexpr int kStageBytes = kTailOffset + 2 * 4096;     // 73,728
+constexpr int kStageBytes = 4 * kChunkBytes + 2 * 4096;  // 73,728 bytes loaded per tile
 constexpr int kMaxThreads = 512;  // producer, 2 MMA issuers, query stager, 2-3 softmax warpgroups
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s
@@ -79,10 +78,24 @@ struct Cfg {
   static constexpr int kQBytes = NQK * kD;
   // query operand buffers: two (the next unit is staged during this one) when they fit
   static constexpr int kQB = (RP == 16) ? 2 : 1;
-  static constexpr int kPBytes = 3 * RP * kTileKeys;
+  // A stage holds one key tile: dims 0..511 as four SW128 chunks of 128 keys x 128 bytes,
+  // then dims 512..575 (the tail, SW64, 128 keys x 64 bytes). At 48 rows each stage also
+  // holds its tile's probabilities (P^T, three e4m3 terms of 6 KB), so the softmax can
+  // write the next tile's P while the values MMA still reads this one: terms 1 and 2 in
+  // 12 KB between the chunks and the tail, term 0 over the first 6 KB of the tail, which
+  // the scores no longer need by then. Otherwise one P buffer serves every tile.
+  static constexpr bool kPInStage = (RP == 48);
+  static constexpr int kPTerm = (RP / 16) * 2048;       // one term: RP/16 groups of 16 rows
+  static constexpr int kTail = 4 * kChunkBytes + (kPInStage ? 2 * kPTerm : 0);
+  static constexpr int kStageStride = kTail + 2 * 4096;
+  static constexpr int kPBytes = kPInStage ? 0 : 3 * kPTerm;
+  // offset of P term t from the P base (the stage's P area, or the shared buffer)
+  static constexpr __host__ __device__ int pterm(int t) {
+    return kPInStage ? ((t + 2) % 3) * kPTerm : t * kPTerm;
+  }
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffStages = 0;
-  static constexpr int kOffP = kStages * kStageBytes;
+  static constexpr int kOffP = kStages * kStageStride;
   static constexpr int kOffQ = kOffP + ((kPBytes + 1023) / 1024) * 1024;
   static constexpr int kOffMisc = kOffQ + kQB * kQBytes;
   static_assert(kTmemUsed <= 512, "TMEM budget");
@@ -95,13 +108,16 @@ struct Misc {
   alignas(16) float row_scale[2][48];  // by unit parity
   alignas(16) float red[2][48 * 4];  // per-tile warp maxima, [row][warp]
   alignas(16) float lred[4][48];
-  alignas(16) float alpha[4][48];    // per-warp copy of this tile's rescale factors
+  alignas(16) float alpha[48];       // this tile's rescale factors (each warp of a
+                                     // warpgroup writes the same values for its rows)
   alignas(16) int grow[2][12];       // per tile parity and warp: some row's max moves
   alignas(16) int row_j[48];         // new-position index j of each row (very negative for padding)
   alignas(16) int row_off[48];       // j * H + h: the row's index among its sequence's rows
   alignas(8) uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, pv_done;
+  uint64_t p_full[2];   // P of tile g is written: p_full[g % 2] (the softmax may run a tile
+                        // ahead of the value MMAs when P lives in the stage)
+  uint64_t pv_done[2];  // PV of tile g completes pv_done[g % 2]
   uint64_t q_full[2];   // query operand buffer holds its unit's terms
   uint64_t q_empty[2];  // the unit that used the buffer has finished its scores
   uint64_t q0_done;     // the first unit's query rows are staged (by warps 2.. together)
@@ -127,6 +143,8 @@ template <int RP>
 constexpr int smem_bytes() {
   return Cfg<RP>::kOffMisc + (int)sizeof(Misc) + 1024;
 }
+static_assert(smem_bytes<16>() <= 232448 && smem_bytes<32>() <= 232448 && smem_bytes<48>() <= 232448,
+              "dynamic shared memory per CTA");
 
 struct DecodeArgs {
   AttnParams p;
@@ -417,8 +435,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       mbar_init(&ms->s_empty[s], 128 * C::kNWG);
     }
     for (int w = 0; w < C::kNWG; ++w) mbar_init(&ms->wg_bar[w], 128);
-    mbar_init(&ms->p_full, 128 * C::kNWG);
-    mbar_init(&ms->pv_done, 1);
+    mbar_init(&ms->p_full[0], 128 * C::kNWG);
+    mbar_init(&ms->p_full[1], 128 * C::kNWG);
+    mbar_init(&ms->pv_done[0], 1);
+    mbar_init(&ms->pv_done[1], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->q_full[s], 1);
       mbar_init(&ms->q_empty[s], 1);
@@ -605,7 +625,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           const int s = fill % kStages;
           const uint32_t n = fill / kStages;
           if (!wait_or_abort(&ms->kv_empty[s], (n & 1) ^ 1, ms, p)) break;
-          uint8_t* st = smem + C::kOffStages + s * kStageBytes;
+          uint8_t* st = smem + C::kOffStages + s * C::kStageStride;
           mbar_arrive_expect_tx(&ms->kv_full[s], kStageBytes);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -623,7 +643,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             for (int c = 0; c < 4; ++c)
               tma_load_2d_hint(st + c * kChunkBytes + h * 8192, &map_main, c * 128, y,
                                &ms->kv_full[s], read_once);
-            tma_load_2d_hint(st + kTailOffset + h * 4096, &map_tail, 0, y, &ms->kv_full[s], read_once);
+            tma_load_2d_hint(st + C::kTail + h * 4096, &map_tail, 0, y, &ms->kv_full[s], read_once);
           }
           ++fill;
           prefetch_upto(fill + kPrefetchTiles);
@@ -642,7 +662,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, 128, C::NQK);
       const uint64_t a_main0 = smem_desc(smem_addr(smem + C::kOffStages), 16, 1024, Swizzle::k128B);
-      const uint64_t a_tail0 = smem_desc(smem_addr(smem + C::kOffStages + kTailOffset), 16, 512, Swizzle::k64B);
+      const uint64_t a_tail0 = smem_desc(smem_addr(smem + C::kOffStages + C::kTail), 16, 512, Swizzle::k64B);
       const uint64_t b_main0 = smem_desc(smem_addr(qbuf), 16, 1024, Swizzle::k128B);
       const uint64_t b_tail0 = smem_desc(smem_addr(qbuf + 4 * (C::NQK * 128)), 16, 512, Swizzle::k64B);
       uint32_t g = 0, units_done = 0;
@@ -658,7 +678,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           if (!(ok = wait_or_abort(&ms->kv_full[s], (g / kStages) & 1, ms, p))) break;
           if (!(ok = wait_or_abort(&ms->s_empty[sb], ((g / C::kSBuf) & 1) ^ 1, ms, p))) break;
           tc_fence_after();
-          const uint32_t soff = (uint32_t)(s * kStageBytes) >> 4;
+          const uint32_t soff = (uint32_t)(s * C::kStageStride) >> 4;
           const uint32_t d = tmem + C::kSCol + sb * C::NQK;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -686,16 +706,19 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       constexpr uint32_t idesc_stacked = instr_desc(0, 0, 1, 1, 128, 3 * RP);
       constexpr uint32_t idesc_term = instr_desc(0, 0, 1, 1, 128, RP);
       const uint64_t a0 = smem_desc(smem_addr(smem + C::kOffStages), kChunkBytes, 1024, Swizzle::k128B);
-      const uint64_t b0 = smem_desc(smem_addr(pbuf), 128, 2048, Swizzle::kNone);
+      // P^T of stage 0's tile (at 48 rows; each stage has its own) or the shared buffer
+      const uint64_t b0 = smem_desc(smem_addr(C::kPInStage ? smem + C::kOffStages + 4 * kChunkBytes : pbuf),
+                                    128, 2048, Swizzle::kNone);
       uint32_t g = 0;
       bool ok = true;
       for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && ok; cu = next_unit(args, cu)) {
         const int n = tiles_in(unit_info(args, ms, cu));
         for (int t = 0; t < n; ++t, ++g) {
-          if (!(ok = wait_or_abort(&ms->p_full, g & 1, ms, p))) break;
+          if (!(ok = wait_or_abort(&ms->p_full[g & 1], (g >> 1) & 1, ms, p))) break;
           tc_fence_after();
           const int s = g % kStages;
-          const uint32_t soff = (uint32_t)(s * kStageBytes) >> 4;
+          const uint32_t soff = (uint32_t)(s * C::kStageStride) >> 4;
+          const uint32_t poff = C::kPInStage ? soff : 0u;
           // consecutive MMAs go to different dv chunks' accumulators where they can
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
@@ -706,17 +729,17 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 const uint64_t a = a0 + soff + ((c * kChunkBytes + ks * 4096) >> 4);
                 if (C::oterms(c) == 3) {  // stacked: one MMA over all three terms' rows
                   if (term == 0)
-                    mma_f8f6f4(tmem + C::ocol(c), a, b0 + ((ks * 512) >> 4), idesc_stacked,
+                    mma_f8f6f4(tmem + C::ocol(c), a, b0 + poff + ((ks * 512) >> 4), idesc_stacked,
                                t > 0 || ks > 0);
                 } else {  // summed: one MMA per term into the same accumulator
-                  mma_f8f6f4(tmem + C::ocol(c), a, b0 + ((term * (RP / 16) * 2048 + ks * 512) >> 4),
+                  mma_f8f6f4(tmem + C::ocol(c), a, b0 + poff + ((C::pterm(term) + ks * 512) >> 4),
                              idesc_term, t > 0 || ks > 0 || term > 0);
                 }
               }
             }
           }
           mma_commit(&ms->kv_empty[s]);
-          mma_commit(&ms->pv_done);
+          mma_commit(&ms->pv_done[g & 1]);
         }
       }
     }
@@ -769,7 +792,17 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     const int i = wq * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
     const float kv_scale = p.kv_scale;
-    uint32_t tile = 0, pv_waits = 0, wg_phase = 0, k = 0;  // k: units with work, in order
+    uint32_t tile = 0, wg_phase = 0, k = 0;  // k: units with work, in order
+    // PV completions are confirmed in tile order, each before the PV two tiles later can
+    // complete (that one needs this warpgroup's next P), so a phase parity names one tile
+    int pv_seen = -1;
+    auto wait_pv_upto = [&](int target) -> bool {
+      for (int g = pv_seen + 1; g <= target; ++g) {
+        if (!wait_or_abort(&ms->pv_done[g & 1], (g >> 1) & 1, ms, p)) return false;
+        pv_seen = g;
+      }
+      return true;
+    };
     uint64_t* wg_bar = &ms->wg_bar[wg];
     // Bounded warpgroup barrier: every thread arrives, then waits for the phase.
     auto wg_sync = [&]() -> bool {
@@ -872,7 +905,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
               l[r] *= al;
               m[r] = tm;
             }
-            if (lane == 0) ms->alpha[wq][rb + r] = al;
+            if (lane == 0) ms->alpha[rb + r] = al;
           }
         }
 #pragma unroll
@@ -902,14 +935,18 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             w3[wi] |= c3 << 16;
           }
         }
-        // the previous tile's PV must be done before P and O are touched
-        if (t > 0) {
-          if (!(ok = wait_or_abort(&ms->pv_done, pv_waits & 1, ms, p))) break;
-          ++pv_waits;
+        // The previous tile's PV must be done before O is rescaled, and before P is written
+        // when one P buffer serves every tile. With P in the stage, PV(tile - 2) is known
+        // done (this tile's keys replaced its stage) and is only confirmed here.
+        {
+          const int upto = (int)tile - ((C::kPInStage && !need_rescale) ? 2 : 1);
+          if (!(ok = wait_pv_upto(upto))) break;
           tc_fence_after();
+        }
+        if (t > 0) {
           if (need_rescale) {
             __syncwarp();
-            const float* al = &ms->alpha[wq][rb];
+            const float* al = &ms->alpha[rb];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -931,7 +968,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
         // keys past this unit's range: zero their V bytes so 0 * garbage cannot be NaN
         if (wg == 0 && kabs >= un.key_hi) {
-          uint8_t* st = smem + C::kOffStages + s * kStageBytes + (i >> 6) * 8192 + (i & 63) * 128;
+          uint8_t* st = smem + C::kOffStages + s * C::kStageStride + (i >> 6) * 8192 + (i & 63) * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -939,20 +976,21 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
               reinterpret_cast<uint4*>(st + c * kChunkBytes)[e] = make_uint4(0, 0, 0, 0);
         }
         // P^T: MN-major, 16 rows x 8 keys core matrices; term t, row group g at
-        // (t * RP/16 + g) * 2048, key i at (i / 8) * 128 + (i % 8) * 16, row r at byte r % 16.
+        // pterm(t) + g * 2048, key i at (i / 8) * 128 + (i % 8) * 16, row r at byte r % 16.
         // This warpgroup writes its rows 8 at a time (8-byte halves of the 16-byte rows).
+        uint8_t* pb = C::kPInStage ? smem + C::kOffStages + s * C::kStageStride + 4 * kChunkBytes : pbuf;
         const int off = (i >> 3) * 128 + (i & 7) * 16;
 #pragma unroll
         for (int blk = 0; blk < RH / 8; ++blk) {
           const int row0 = rb + 8 * blk;
           const int o = (row0 >> 4) * 2048 + off + ((row0 & 15) >> 3) * 8;
-          *reinterpret_cast<uint2*>(pbuf + 0 * (RP / 16) * 2048 + o) = make_uint2(w1[2 * blk], w1[2 * blk + 1]);
-          *reinterpret_cast<uint2*>(pbuf + 1 * (RP / 16) * 2048 + o) = make_uint2(w2[2 * blk], w2[2 * blk + 1]);
-          *reinterpret_cast<uint2*>(pbuf + 2 * (RP / 16) * 2048 + o) = make_uint2(w3[2 * blk], w3[2 * blk + 1]);
+          *reinterpret_cast<uint2*>(pb + C::pterm(0) + o) = make_uint2(w1[2 * blk], w1[2 * blk + 1]);
+          *reinterpret_cast<uint2*>(pb + C::pterm(1) + o) = make_uint2(w2[2 * blk], w2[2 * blk + 1]);
+          *reinterpret_cast<uint2*>(pb + C::pterm(2) + o) = make_uint2(w3[2 * blk], w3[2 * blk + 1]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&ms->p_full);
+        mbar_arrive(&ms->p_full[tile & 1]);
       }
       if (!ok) break;
       // ---- epilogue: row sums, then O / l
@@ -971,8 +1009,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         l[r] = lt;
         inv[r] = lt > 0.f ? kv_scale / lt : 0.f;
       }
-      if (!(ok = wait_or_abort(&ms->pv_done, pv_waits & 1, ms, p))) break;
-      ++pv_waits;
+      if (!(ok = wait_pv_upto((int)tile - 1))) break;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
