@@ -375,6 +375,30 @@ def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
     res["causal_prefill"] = {"ms_per_chunk": ms, "tok_s": inp.n_q / (ms / 1e3), "TFLOP_s": tf,
                              "frac_of_bf16_peak": tf / bf16_peak,
                              "algorithmic_flops": flops, "T": inp.n_q, "prefix": 32768, "H": inp.H}
+    del kv, q, out, lse, ws
+    # appending new rows to the cache: a prefill chunk's 8,192 rows and a decode step's 32,
+    # into a pool larger than L2 (each call writes a different set of slots)
+    g = torch.Generator().manual_seed(7)
+    pool = torch.zeros(8192, 64, 576, dtype=torch.uint8, device=dev)  # 302 MB
+    for name, n in (("cache_append_prefill_chunk", 8192), ("cache_append_decode_step", 32)):
+        x = (torch.randn(n, 576, generator=g)).to(torch.bfloat16).to(dev)
+        slot_sets = [torch.randperm(pool.shape[0] * 64, generator=g)[:n].to(dev) for _ in range(8)]
+        # device time: the calls captured in a CUDA graph and replayed (a single small call
+        # is otherwise dominated by the host-side launch path)
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            for i in range(8):
+                mla.mla_cache_append(pool, x, slot_sets[i], 0.0125)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(16):
+                mla.mla_cache_append(pool, x, slot_sets[i % 8], 0.0125)
+        ms = _time_events(lambda i: graph.replay(), max(3, steps // 5), 2) / 16
+        nbytes = n * (576 * 2 + 576 + 8)  # bf16 rows in, codes out, slots
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"us_per_call": ms * 1e3, "GB_s": gbs, "frac_of_hbm_peak": gbs / hbm_peak,
+                     "rows": n, "algorithmic_bytes": nbytes}
     return res
 
 

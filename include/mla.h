@@ -146,6 +146,27 @@ mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, 
                            void* out, float* lse, void* stream);
 
 /*
+ * Append new latent rows to the paged cache ("MI355X Kimi K2.5 vLLM AITER 7x speedup",
+ * section "PR #35850 修复了什么": the FP8 KV cache handled natively; "Scaling Kimi K3 ...",
+ * section "缓存可复用，还要能一致地恢复": 576 FP8 bytes per position). For every i < n with
+ * slots[i] >= 0, cache row slots[i] (page slots[i] / page_size, position slots[i] %
+ * page_size) becomes the e4m3 codes of x_i * (1 / kv_scale): the reciprocal and each
+ * product are rounded to binary32, the conversion rounds to nearest even and saturates
+ * finite values and infinities at +-448 (NaN stays NaN). Rows with a negative slot are
+ * skipped (padding).
+ *   pool    device, [num_pages][page_size][576] e4m3 codes, 16-byte aligned (written)
+ *   x       device, [n][576] bfloat16, 16-byte aligned
+ *   slots   device, [n] int64 flat cache rows, 8-byte aligned
+ *   kv_scale the cache's per-tensor scale (> 0, finite)
+ *   status  device word or NULL: set to MLA_ERR_BOUNDS (if it held 0) when a slot is not
+ *           below num_pages * page_size; that row is not written
+ * Rows are written in no particular order: two rows with the same slot leave one of them.
+ */
+mla_status_t mla_cache_append(uint8_t* pool, int64_t num_pages, int32_t page_size,
+                              const void* x, const int64_t* slots, int64_t n, float kv_scale,
+                              unsigned* status, void* stream);
+
+/*
  * Synchronises `stream`, then returns the status the last call on this workspace left
  * (MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT: the first non-zero of the words its CTAs
  * wrote at exit), or MLA_ERR_CUDA if the stream itself reports an error.

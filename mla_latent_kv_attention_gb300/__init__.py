@@ -28,7 +28,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 # Every symbol include/mla.h declares.
 EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse",
            "mla_read_status", "mla_status_string", "mla_last_launch_count",
-           "mla_set_profile_events", "mla_decode_static_ws")
+           "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append")
 
 
 class MlaError(RuntimeError):
@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_set_profile_events.restype = None
     lib.mla_decode_static_ws.argtypes = [KV, P, i32, i32, f32, P, P, P]
     lib.mla_decode_static_ws.restype = i32
+    lib.mla_cache_append.argtypes = [P, i64, i32, P, P, i64, f32, P, P]
+    lib.mla_cache_append.restype = i32
     for name in ("mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse", "mla_read_status",
                  "mla_last_launch_count"):
         getattr(lib, name).restype = i32
@@ -205,6 +207,23 @@ def mla_merge_lse(part_out: torch.Tensor, part_lse: torch.Tensor, out=None, lse=
     _check("mla_merge_lse", library().mla_merge_lse(part_out.data_ptr(), part_lse.data_ptr(), S, R,
                                                out.data_ptr(), _ptr(lse), _stream(stream)))
     return out, lse
+
+
+def mla_cache_append(pool: torch.Tensor, x: torch.Tensor, slots: torch.Tensor, kv_scale: float,
+                     status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Write bf16 rows x [n, 576] into the uint8 pool [num_pages, page_size, 576] as e4m3
+    codes of x / kv_scale at flat rows `slots` (int64 [n]; negative = skip). `status`, an
+    int32 CUDA tensor of one element, receives MLA_ERR_BOUNDS for a slot past the pool."""
+    if pool.dtype != torch.uint8 or pool.dim() != 3 or pool.shape[2] != MLA_D or not pool.is_contiguous():
+        raise ValueError("pool must be a contiguous uint8 tensor [num_pages, page_size, 576]")
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != MLA_D or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bfloat16 tensor [n, 576]")
+    if slots.dtype != torch.int64 or slots.dim() != 1 or slots.shape[0] != x.shape[0]:
+        raise ValueError("slots must be an int64 tensor [n]")
+    _check("mla_cache_append", library().mla_cache_append(
+        pool.data_ptr(), pool.shape[0], pool.shape[1], x.data_ptr(), slots.data_ptr(),
+        x.shape[0], float(kv_scale), None if status is None else status.data_ptr(),
+        _stream(stream)))
 
 
 def mla_read_status(ws: torch.Tensor, stream=None) -> int:

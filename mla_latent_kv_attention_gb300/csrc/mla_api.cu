@@ -1,5 +1,6 @@
 // mla_api.cu -- the C ABI of libmla: argument checks, workspace layout, launches.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "mla_internal.cuh"
@@ -193,6 +194,32 @@ mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, 
   if (mla::launch_merge_standalone(part_out, part_lse, S, R, static_cast<uint16_t*>(out), lse, sms,
                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
+  ++g_last_launches;
+  return MLA_OK;
+}
+
+mla_status_t mla_cache_append(uint8_t* pool, int64_t num_pages, int32_t page_size,
+                              const void* x, const int64_t* slots, int64_t n, float kv_scale,
+                              unsigned* status, void* stream) {
+  g_last_launches = 0;
+  if (n < 0 || num_pages < 0 || page_size <= 0) return MLA_ERR_INVALID_ARG;
+  if (!(kv_scale > 0.f) || !(kv_scale < INFINITY)) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (!pool || !x || !slots) return MLA_ERR_INVALID_ARG;
+  if (!aligned(pool, 16) || !aligned(x, 16) || !aligned(slots, 8) || (status && !aligned(status, 4)))
+    return MLA_ERR_INVALID_ARG;
+  int dev;
+  mla_status_t st = current_device(&dev);
+  if (st != MLA_OK) return st;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const float inv = 1.0f / kv_scale;  // binary32, as the definition states
+  if (mla::launch_cache_append(pool, num_pages * (int64_t)page_size, static_cast<const uint16_t*>(x),
+                               slots, n, inv, status, sms, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   ++g_last_launches;
   return MLA_OK;
 }

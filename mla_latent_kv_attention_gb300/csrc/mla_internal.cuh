@@ -127,5 +127,8 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
 cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
                                     uint16_t* out, float* lse, int num_sms, cudaStream_t s);
+cudaError_t launch_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t* x,
+                                const int64_t* slots, int64_t n, float inv, unsigned* status,
+                                int num_sms, cudaStream_t s);
 
 }  // namespace mla

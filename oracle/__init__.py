@@ -70,6 +70,10 @@ def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attention_range.restype = i32
     lib.oracle_merge_lse.argtypes = [P, P, i32, i64, P, P]
     lib.oracle_merge_lse.restype = None
+    lib.oracle_e4m3_encode.argtypes = [dbl]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_cache_append.argtypes = [P, i64, P, P, i64, ctypes.c_float]
+    lib.oracle_cache_append.restype = i32
     return lib
 
 
@@ -170,3 +174,24 @@ def merge_lse(part_out, part_lse):
     lse = np.empty((R,), dtype=np.float64)
     lib.oracle_merge_lse(_ptr(po), _ptr(pl), S, R, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def e4m3_encode(v: float) -> int:
+    """e4m3fn code nearest to v (ties to even, saturating at +-448)."""
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def cache_append(pool, x, slots, kv_scale: float):
+    """Append bf16 rows x [n, 576] to a copy of the paged pool (uint8 [num_pages, page_size,
+    576] or [rows, 576]) at flat row slots [n] (negative: skipped). Returns the new pool
+    (numpy uint8, same shape); raises if a slot is past the pool."""
+    lib = _load()
+    pool_np = _np(pool, np.uint8).copy()
+    xs = _np(x, np.uint16)
+    sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int64))
+    rows = pool_np.size // 576
+    rc = lib.oracle_cache_append(_ptr(pool_np), rows, _ptr(xs), _ptr(sl), sl.shape[0],
+                                 float(kv_scale))
+    if rc != 0:
+        raise ValueError("oracle_cache_append: slot past the end of the pool")
+    return pool_np

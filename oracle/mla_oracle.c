@@ -206,3 +206,44 @@ void oracle_merge_lse(const double* part_out, const double* part_lse, int S, int
     lse[r] = l;
   }
 }
+
+/* Nearest finite e4m3 value by exhaustive comparison with the 127 non-negative codes
+ * 0x00..0x7E (0x7F is NaN); a tie goes to the even code, whose mantissa bit 0 is clear. */
+uint8_t oracle_e4m3_encode(double v) {
+  if (isnan(v)) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  double a = fabs(v);
+  if (a > 448.0) a = 448.0;
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    const double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+int oracle_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t* x_bf16,
+                        const int64_t* slots, int64_t n, float kv_scale) {
+  /* binary32 arithmetic as the definition states (C evaluates float * float in float on the
+     targets this is built for: FLT_EVAL_METHOD 0) */
+  const float inv = 1.0f / kv_scale;
+  int rc = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t s = slots[i];
+    if (s < 0) continue;
+    if (s >= pool_rows) {
+      rc = -1;
+      continue;
+    }
+    for (int d = 0; d < ORACLE_D; ++d) {
+      const float x = (float)oracle_bf16_value(x_bf16[i * ORACLE_D + d]);
+      const float prod = x * inv;
+      pool[s * ORACLE_D + d] = oracle_e4m3_encode((double)prod);
+    }
+  }
+  return rc;
+}

@@ -76,6 +76,24 @@ int oracle_attention_range(const uint8_t* pool, int64_t num_pages, int page_size
 void oracle_merge_lse(const double* part_out, const double* part_lse, int S, int64_t R,
                       double* out, double* lse);
 
+/*
+ * e4m3fn code of the finite value nearest to v, ties to the code with the even mantissa
+ * bit; |v| > 448 (and +-inf) saturate to +-448; the sign bit is v's (so -0 gives 0x80);
+ * NaN gives 0x7F. Found by comparing v with the value of every finite code (the encoding
+ * is the inverse of oracle_e4m3_value on the representable values).
+ */
+uint8_t oracle_e4m3_encode(double v);
+
+/*
+ * Append new latent rows to a paged FP8 cache: for each i < n with slots[i] >= 0,
+ *   pool row slots[i] (byte offset slots[i] * 576) <- e4m3_encode(x_i[d] * inv), d < 576,
+ * where inv = 1 / kv_scale and the product are both rounded to binary32 (round to nearest
+ * even), x_i being the bfloat16 row i. Rows with a negative slot are skipped.
+ * Returns 0, or -1 if a slot is not below pool_rows (nothing is written for that row).
+ */
+int oracle_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t* x_bf16,
+                        const int64_t* slots, int64_t n, float kv_scale);
+
 #ifdef __cplusplus
 }
 #endif

@@ -253,8 +253,68 @@ def pin_sampled_rows(orc):
         assert np.array_equal(o[i], out[b, j, h]) and l[i] == lse[b, j, h]
 
 
+def pin_e4m3_encode(orc):
+    """The encoder against the decoder, the OCP rounding rule and torch's float8_e4m3fn
+    conversion: every finite code (both signs, zero, subnormals) encodes back to itself;
+    the midpoint of two neighbouring codes goes to the one with the even mantissa bit and
+    any point off the midpoint to the nearer one; magnitudes past 448 and infinities
+    saturate, -0 keeps its sign, NaN gives 0x7F; random binary32 values within +-448 give
+    torch's codes (round to nearest even)."""
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert orc.e4m3_encode(orc.e4m3_value(c)) == c, c
+    for c in range(0x7E):
+        lo, hi = orc.e4m3_value(c), orc.e4m3_value(c + 1)
+        mid, eps = (lo + hi) / 2, (hi - lo) * 1e-3
+        even = c if c % 2 == 0 else c + 1
+        assert orc.e4m3_encode(mid) == even, c
+        assert orc.e4m3_encode(-mid) == 0x80 | even, c
+        assert orc.e4m3_encode(mid - eps) == c and orc.e4m3_encode(mid + eps) == c + 1, c
+    for v, code in ((448.0, 0x7E), (464.0, 0x7E), (1e6, 0x7E), (-1e6, 0xFE), (math.inf, 0x7E),
+                    (-math.inf, 0xFE), (0.0, 0x00), (-0.0, 0x80), (2.0 ** -10, 0x00),
+                    (1.5 * 2.0 ** -10, 0x01)):
+        assert orc.e4m3_encode(v) == code, (v, code)
+    assert orc.e4m3_encode(math.nan) == 0x7F
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(20000, generator=g) * torch.exp(torch.randn(20000, generator=g) * 3)
+    x = x.clamp(-448, 448)
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).tolist()
+    mine = [orc.e4m3_encode(float(v)) for v in x.tolist()]
+    assert mine == ref
+
+
+def pin_cache_append(orc):
+    """Appending rows against torch: a written row holds torch's float8_e4m3fn codes of the
+    binary32 product x * (1/kv_scale) (saturated at +-448); rows with a negative slot and
+    rows nobody writes stay as they were; a slot past the pool is refused."""
+    g = torch.Generator().manual_seed(6)
+    pool = torch.randint(0, 256, (6, 4, D), dtype=torch.uint8, generator=g)  # 24 rows
+    x = (torch.randn(5, D, generator=g) * 3).to(torch.bfloat16)
+    x[0, :4] = torch.tensor([1e30, -1e30, float("inf"), -0.0]).to(torch.bfloat16)
+    slots = [3, -1, 23, 0, 10]
+    scale = 0.0173
+    new = orc.cache_append(pool, x, slots, scale).reshape(-1, D)
+    old = pool.reshape(-1, D).numpy()
+    inv = torch.tensor(1.0, dtype=torch.float32) / torch.tensor(scale, dtype=torch.float32)
+    for r in range(old.shape[0]):
+        if r not in slots:
+            assert (new[r] == old[r]).all(), r
+    for i, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        prod = (x[i].float() * inv).clamp(-448, 448)
+        ref = prod.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert (new[slot] == ref).all(), i
+    try:
+        orc.cache_append(pool, x[:1], [24], scale)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a slot past the pool was accepted")
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_bf16, pin_brute_force_sdpa, pin_constant_v, pin_single_key,
     pin_zero_query, pin_duplicate_key, pin_split_merge, pin_merge_weights, pin_permuted_pages,
-    pin_head_padding_and_permutation, pin_causal_prefix, pin_sampled_rows,
+    pin_head_padding_and_permutation, pin_causal_prefix, pin_sampled_rows, pin_e4m3_encode,
+    pin_cache_append,
 ]

@@ -94,3 +94,26 @@ def test_workspace_size_rejects_unsupported():
 def test_read_status_rejects_small_workspace():
     lib = mla.library()
     assert lib.mla_read_status(FAKE, 4, None) == 3
+
+
+def test_cache_append_rejects_bad_arguments():
+    lib = mla.library()
+    ok = dict(pool=FAKE, num_pages=4, page_size=64, x=FAKE, slots=FAKE, n=3, kv_scale=0.5,
+              status=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.mla_cache_append(a["pool"], a["num_pages"], a["page_size"], a["x"], a["slots"],
+                                    a["n"], a["kv_scale"], a["status"], None)
+
+    assert call(n=-1) == 1
+    assert call(page_size=0) == 1
+    assert call(kv_scale=0.0) == 1
+    assert call(kv_scale=float("inf")) == 1
+    assert call(kv_scale=float("nan")) == 1
+    assert call(pool=None) == 1
+    assert call(x=FAKE + 8) == 1      # bf16 rows are read 16 bytes at a time
+    assert call(slots=FAKE + 4) == 1  # int64 slots
+    assert call(status=FAKE + 2) == 1
+    assert call(n=0, pool=None, x=None, slots=None) == 0  # nothing to do
+    assert lib.mla_last_launch_count() == 0

@@ -34,6 +34,12 @@ MUTANTS = {
     "kv_scale_dropped": ("table[c] = oracle_e4m3_value((uint8_t)c) * kv_scale;",
                          "table[c] = oracle_e4m3_value((uint8_t)c);"),
     "e4m3_nan_code": ("if (e == 0xF && m == 0x7) return NAN;", "if (e == 0xF && m == 0x6) return NAN;"),
+    "encode_ties_up": ("(err == best_err && (c & 1) == 0 && (best & 1) == 1)", "(err == best_err)"),
+    "encode_drops_sign": ("const uint8_t sign = signbit(v) ? 0x80 : 0x00;",
+                          "const uint8_t sign = v < 0 ? 0x80 : 0x00;"),
+    "encode_no_saturation": ("if (a > 448.0) a = 448.0;", ""),
+    "append_scale_not_inverted": ("const float prod = x * inv;", "const float prod = x * kv_scale;"),
+    "append_row_offset": ("pool[s * ORACLE_D + d] =", "pool[(s + 1) * ORACLE_D + d - ORACLE_D * (s == pool_rows - 1)] ="),
 }
 
 
