@@ -399,6 +399,20 @@ def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
         gbs = nbytes / (ms / 1e3) / 1e9
         res[name] = {"us_per_call": ms * 1e3, "GB_s": gbs, "frac_of_hbm_peak": gbs / hbm_peak,
                      "rows": n, "algorithmic_bytes": nbytes}
+    del pool
+    # top-k renormalisation of the probability rows of a decode batch: 32 rows over a
+    # 129,280-entry vocabulary, per-row k, sets rotated to exceed L2
+    B, V = 32, 129280
+    copies = max(2, math.ceil(3 * l2 / (B * V * 8)))
+    psets = [torch.softmax(torch.randn(B, V, generator=g) * 3, dim=1).to(dev) for _ in range(copies)]
+    outs = [torch.empty_like(p) for p in psets]
+    ks = torch.randint(1, 1024, (B,), generator=g, dtype=torch.int32).to(dev)
+    ms = _time_events(lambda i: mla.mla_top_k_renorm_prob(psets[i % copies], ks, out=outs[i % copies]),
+                      steps, 3)
+    nbytes = B * V * 4 * 2  # rows read once, written once
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res["top_k_renorm_prob"] = {"us_per_call": ms * 1e3, "GB_s": gbs, "frac_of_hbm_peak": gbs / hbm_peak,
+                                "B": B, "V": V, "algorithmic_bytes": nbytes}
     return res
 
 

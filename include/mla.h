@@ -167,6 +167,20 @@ mla_status_t mla_cache_append(uint8_t* pool, int64_t num_pages, int32_t page_siz
                               unsigned* status, void* stream);
 
 /*
+ * Top-k renormalisation of probability rows, the sampling step of speculative-verify
+ * acceptance ("MI355X Kimi K2.5 vLLM AITER 7x speedup": top_k_renorm_prob among the
+ * serving stack's sampling kernels). Per row r with k_r = top_k ? top_k[r] : k:
+ * pivot = the k_r-th largest probability; every p >= pivot is kept (ties at the pivot
+ * included), out = p / (sum of the kept entries), the rest 0. k_r <= 0 or k_r >= V keeps
+ * the whole row. Probabilities must be non-negative and finite.
+ *   probs  device, [B][V] float32 (read)
+ *   out    device, [B][V] float32 (written; may not alias probs)
+ *   top_k  device, [B] int32, or NULL to use k for every row
+ */
+mla_status_t mla_top_k_renorm_prob(const float* probs, float* out, int B, int V,
+                                   const int32_t* top_k, int k, void* stream);
+
+/*
  * Synchronises `stream`, then returns the status the last call on this workspace left
  * (MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT: the first non-zero of the words its CTAs
  * wrote at exit), or MLA_ERR_CUDA if the stream itself reports an error.

@@ -28,7 +28,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 # Every symbol include/mla.h declares.
 EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse",
            "mla_read_status", "mla_status_string", "mla_last_launch_count",
-           "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append")
+           "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append",
+           "mla_top_k_renorm_prob")
 
 
 class MlaError(RuntimeError):
@@ -69,6 +70,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_static_ws.restype = i32
     lib.mla_cache_append.argtypes = [P, i64, i32, P, P, i64, f32, P, P]
     lib.mla_cache_append.restype = i32
+    lib.mla_top_k_renorm_prob.argtypes = [P, P, i32, i32, P, i32, P]
+    lib.mla_top_k_renorm_prob.restype = i32
     for name in ("mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse", "mla_read_status",
                  "mla_last_launch_count"):
         getattr(lib, name).restype = i32
@@ -224,6 +227,25 @@ def mla_cache_append(pool: torch.Tensor, x: torch.Tensor, slots: torch.Tensor, k
         pool.data_ptr(), pool.shape[0], pool.shape[1], x.data_ptr(), slots.data_ptr(),
         x.shape[0], float(kv_scale), None if status is None else status.data_ptr(),
         _stream(stream)))
+
+
+def mla_top_k_renorm_prob(probs: torch.Tensor, top_k, out: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """probs float32 [B, V] -> top-k renormalised copy; top_k an int (all rows) or an int32
+    CUDA tensor [B]."""
+    if probs.dtype != torch.float32 or probs.dim() != 2 or not probs.is_contiguous():
+        raise ValueError("probs must be a contiguous float32 tensor [B, V]")
+    B, V = probs.shape
+    out = torch.empty_like(probs) if out is None else out
+    if isinstance(top_k, torch.Tensor):
+        if top_k.dtype != torch.int32 or top_k.shape != (B,):
+            raise ValueError("top_k must be an int32 tensor [B]")
+        kp, k = top_k.data_ptr(), 0
+    else:
+        kp, k = None, int(top_k)
+    _check("mla_top_k_renorm_prob", library().mla_top_k_renorm_prob(
+        probs.data_ptr(), out.data_ptr(), B, V, kp, k, _stream(stream)))
+    return out
 
 
 def mla_read_status(ws: torch.Tensor, stream=None) -> int:

@@ -224,6 +224,22 @@ mla_status_t mla_cache_append(uint8_t* pool, int64_t num_pages, int32_t page_siz
   return MLA_OK;
 }
 
+mla_status_t mla_top_k_renorm_prob(const float* probs, float* out, int B, int V,
+                                   const int32_t* top_k, int k, void* stream) {
+  g_last_launches = 0;
+  if (B < 0 || V < 0) return MLA_ERR_INVALID_ARG;
+  if (B == 0 || V == 0) return MLA_OK;
+  if (!probs || !out || !aligned(probs, 4) || !aligned(out, 4) || (top_k && !aligned(top_k, 4)))
+    return MLA_ERR_INVALID_ARG;
+  if (mla::launch_top_k_renorm(probs, out, B, V, top_k, k, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  ++g_last_launches;
+  return MLA_OK;
+}
+
 mla_status_t mla_read_status(const void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < sizeof(mla::WsHeader)) return MLA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -130,5 +130,7 @@ cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse
 cudaError_t launch_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t* x,
                                 const int64_t* slots, int64_t n, float inv, unsigned* status,
                                 int num_sms, cudaStream_t s);
+cudaError_t launch_top_k_renorm(const float* probs, float* out, int B, int V, const int32_t* top_k,
+                                int k_all, cudaStream_t s);
 
 }  // namespace mla

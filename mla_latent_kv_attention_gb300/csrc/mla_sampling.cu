@@ -1,0 +1,224 @@
+// mla_sampling.cu -- top-k renormalisation of probability rows for speculative verify.
+//
+// Acceptance sampling after a verify pass draws from the target model's probabilities cut
+// down to the k most likely tokens: keep the k largest entries of each row, zero the rest
+// and rescale the kept ones to sum to one ("AMD MI355X推理Kimi K3：吞吐量超NVIDIA，首字优化显著",
+// section "ROCm适配迎来突破，软件壁垒不再高不可攀"; "在 MI355X 上运行 Kimi K3 的性价比比 B300 更好",
+// the part on how the throughput was reached, which builds it from a sort, a masked fill and
+// a divide). As with a sort and a mask, the cut is by value: pivot = the k-th largest entry,
+// every p_i >= pivot is kept (ties at the pivot are all kept), out_i = p_i / sum of the kept.
+// k <= 0 or k >= V keeps the whole row (out = p / sum p). Entries must be >= 0.
+//
+// A cluster of up to eight CTAs takes one row; each CTA holds its slice of the row in
+// registers (32 entries a thread), so the row is read from memory once and written once.
+// The pivot comes from radix selection on the bit patterns (for non-negative floats the bit
+// pattern orders like the value): up to three passes of 11, 11 and 9 bits below the sign
+// bit, each a count histogram of the next digit of the entries still in play. Every CTA
+// counts its slice into its own shared-memory histogram, the cluster's histograms are added
+// through distributed shared memory, and every CTA selects the bin on the totals. Selection
+// stops early when the bin that holds the k-th largest entry is kept whole. The kept sum is
+// a reduction in the output pass.
+#include <cuda_runtime.h>
+
+#include "mla_internal.cuh"
+#include "sm100.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kTkThreads = 512;
+constexpr int kTkPerThread = 32;                          // register-resident entries a thread
+constexpr int kTkChunk = kTkThreads * kTkPerThread;       // entries a CTA holds (16,384)
+constexpr int kTkMaxCluster = 8;
+constexpr int kBins = 2048;
+constexpr int kWarps = kTkThreads / 32;
+constexpr int kPasses = 3;
+// digit width of a pass, below the sign bit (always 0 in a key): bits 30..20, 19..9, 8..0
+__device__ constexpr int digit_width(int pass) { return pass == kPasses - 1 ? 9 : 11; }
+
+struct __align__(16) TkSmem {
+  unsigned hist[kPasses][kBins];  // this CTA's counts, one buffer a pass (read remotely)
+  unsigned tot[kBins];            // the cluster's counts of the current pass
+  unsigned wsum[kWarps];
+  float wsum_f[kWarps];
+  float part;                     // this CTA's kept sum (read by the other CTAs)
+  int bin;
+  unsigned above, in_bin;
+};
+
+// Largest bin b with count(bins >= b) >= k, from the totals: writes b, the count of the
+// bins above it and its own count. Thread t owns the four bins nbins-4-4t .. nbins-1-4t.
+__device__ void select_bin(TkSmem& s, unsigned k, int nbins) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int lo = nbins - 4 - 4 * t;
+  uint4 c4 = make_uint4(0u, 0u, 0u, 0u);
+  if (lo >= 0) c4 = *reinterpret_cast<const uint4*>(&s.tot[lo]);
+  const unsigned c = c4.x + c4.y + c4.z + c4.w;
+  unsigned incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s.wsum[warp] = incl;
+  __syncthreads();
+  incl += __reduce_add_sync(0xffffffffu, lane < warp ? s.wsum[lane] : 0u);
+  unsigned a = incl - c;  // count of the bins above this thread's
+  if (a < k && incl >= k) {
+    const unsigned v[4] = {c4.w, c4.z, c4.y, c4.x};  // from the top
+    int j = 0;
+    while (a + v[j] < k) a += v[j++];
+    s.bin = lo + 3 - j;
+    s.above = a;
+    s.in_bin = v[j];
+  }
+  __syncthreads();
+}
+
+// Sum over the block of one float a thread; the result is valid in every thread.
+__device__ __forceinline__ float block_sum(TkSmem& s, float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) s.wsum_f[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += s.wsum_f[w];
+  return t;
+}
+
+__global__ void __launch_bounds__(kTkThreads, 2)
+    top_k_renorm_kernel(const float* __restrict__ probs, float* __restrict__ out, int V, int n,
+                        const int32_t* __restrict__ top_k, int k_all) {
+  __shared__ TkSmem s;
+  const int t = threadIdx.x, lane = t & 31;
+  const unsigned rank = sm100::cluster_ctarank();
+  const int64_t row = blockIdx.x / n;
+  const float* p = probs + row * (int64_t)V;
+  float* o = out + row * (int64_t)V;
+  // this CTA's register slice: entries rank * kTkChunk + j * kTkThreads + t; entries past
+  // the register slices of the cluster (V > n * kTkChunk, only when n is the maximum) are
+  // re-read from memory in every pass, warp by warp.
+  const int64_t base = (int64_t)rank * kTkChunk + t;
+  const int64_t tail0 = (int64_t)n * kTkChunk + (int64_t)rank * kTkThreads + (t & ~31);
+  const int64_t tail_step = (int64_t)n * kTkThreads;
+  unsigned key[kTkPerThread];  // |p| bit patterns; 0 past the end (counts as a zero entry)
+#pragma unroll
+  for (int j = 0; j < kTkPerThread; ++j) {
+    const int64_t i = base + (int64_t)j * kTkThreads;
+    key[j] = i < V ? (__float_as_uint(__ldcs(p + i)) & 0x7FFFFFFFu) : 0u;
+  }
+  auto tail_key = [&](int64_t i) -> unsigned {
+    return i < V ? (__float_as_uint(__ldcs(p + i)) & 0x7FFFFFFFu) : 0u;
+  };
+  const int kk = top_k ? top_k[row] : k_all;
+  unsigned pivot = 0;  // lowest kept bit pattern; 0 keeps everything
+  if (kk > 0 && kk < V) {
+    // Zero entries past the end of the row only ever add zeros below a positive pivot, and
+    // a pivot of zero keeps the zeros of the row anyway, so they change no selection.
+    for (int b = t; b < kPasses * kBins; b += kTkThreads) (&s.hist[0][0])[b] = 0u;
+    __syncthreads();
+    unsigned k = (unsigned)kk, prefix = 0;  // prefix: the selected high bits (sign bit first)
+    int done = 1;
+#pragma unroll
+    for (int pass = 0; pass < kPasses; ++pass) {
+      const int wbits = digit_width(pass), shift = 32 - done - wbits, nbins = 1 << wbits;
+      unsigned* hist = s.hist[pass];
+      auto count = [&](unsigned kv) {
+        if ((kv >> (32 - done)) == prefix) atomicAdd(&hist[(kv >> shift) & (unsigned)(nbins - 1)], 1u);
+      };
+#pragma unroll
+      for (int j = 0; j < kTkPerThread; ++j) count(key[j]);
+      for (int64_t i = tail0 + lane; i < V; i += tail_step) count(tail_key(i));
+      sm100::cluster_sync();  // every CTA's histogram of this pass is complete
+      // four bins a thread; the remote loads go out four CTAs at a time, all issued before
+      // the first add
+      for (int b4 = t; b4 < nbins / 4; b4 += kTkThreads) {
+        uint4 c = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int r0 = 0; r0 < kTkMaxCluster; r0 += 4) {
+          uint4 v[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (r0 + r < n) v[r] = sm100::ld_dsmem_v4(&hist[4 * b4], (uint32_t)(r0 + r));
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (r0 + r < n) {
+              c.x += v[r].x;
+              c.y += v[r].y;
+              c.z += v[r].z;
+              c.w += v[r].w;
+            }
+        }
+        *reinterpret_cast<uint4*>(&s.tot[4 * b4]) = c;
+      }
+      __syncthreads();
+      select_bin(s, k, nbins);
+      k -= s.above;
+      prefix = (prefix << wbits) | (unsigned)s.bin;
+      done += wbits;
+      // the k-th largest is the smallest entry of the selected bin when the bin is kept
+      // whole; the kept set is then every key from the bin's lower end up
+      if (k == s.in_bin || pass == kPasses - 1) {
+        pivot = prefix << (32 - done);
+        break;
+      }
+      __syncthreads();  // s.bin / s.above / s.in_bin are read before the next pass writes them
+    }
+  }
+  float kept = 0.f;
+#pragma unroll
+  for (int j = 0; j < kTkPerThread; ++j)
+    if (key[j] >= pivot) kept += __uint_as_float(key[j]);
+  for (int64_t i = tail0 + lane; i < V; i += tail_step) {
+    const unsigned kv = tail_key(i);
+    if (kv >= pivot) kept += __uint_as_float(kv);
+  }
+  kept = block_sum(s, kept);
+  if (t == 0) s.part = kept;
+  sm100::cluster_sync();  // every CTA's part is written (and the last pass's reads are done)
+  float total = 0.f;
+#pragma unroll
+  for (int r0 = 0; r0 < kTkMaxCluster; r0 += 4) {
+    float parts[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      parts[r] = r0 + r < n ? __uint_as_float(sm100::ld_dsmem_u32(&s.part, (uint32_t)(r0 + r))) : 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) total += parts[r];
+  }
+  const float inv = 1.f / total;
+#pragma unroll
+  for (int j = 0; j < kTkPerThread; ++j) {
+    const int64_t i = base + (int64_t)j * kTkThreads;
+    if (i < V) __stcs(o + i, key[j] >= pivot ? __uint_as_float(key[j]) * inv : 0.f);
+  }
+  for (int64_t i = tail0 + lane; i < V; i += tail_step) {
+    const unsigned kv = tail_key(i);
+    __stcs(o + i, kv >= pivot ? __uint_as_float(kv) * inv : 0.f);
+  }
+  sm100::cluster_sync();  // no CTA leaves while another may still read its shared memory
+}
+
+}  // namespace
+
+cudaError_t launch_top_k_renorm(const float* probs, float* out, int B, int V, const int32_t* top_k,
+                                int k_all, cudaStream_t s) {
+  int n = (int)(((int64_t)V + kTkChunk - 1) / kTkChunk);
+  n = n < 1 ? 1 : (n > kTkMaxCluster ? kTkMaxCluster : n);
+  if ((int64_t)B * n > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * n));
+  cfg.blockDim = dim3(kTkThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)n;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, top_k_renorm_kernel, probs, out, V, n, top_k, k_all);
+}
+
+}  // namespace mla

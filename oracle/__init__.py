@@ -195,3 +195,22 @@ def cache_append(pool, x, slots, kv_scale: float):
     if rc != 0:
         raise ValueError("oracle_cache_append: slot past the end of the pool")
     return pool_np
+
+
+def top_k_renorm_prob(probs, top_k):
+    """Row-wise top-k renormalisation in float64, straight from the definition: the pivot is
+    the k-th largest entry (a sort), every entry >= pivot is kept, the kept entries are
+    divided by their sum; k <= 0 or k >= V keeps the row. probs [B, V]; top_k int or [B]."""
+    p = np.asarray(probs, dtype=np.float64)
+    B, V = p.shape
+    ks = np.broadcast_to(np.asarray(top_k, dtype=np.int64), (B,))
+    out = np.zeros_like(p)
+    for r in range(B):
+        k = int(ks[r])
+        if k <= 0 or k >= V:
+            keep = np.ones(V, dtype=bool)
+        else:
+            pivot = np.sort(p[r])[V - k]
+            keep = p[r] >= pivot
+        out[r, keep] = p[r, keep] / p[r, keep].sum()
+    return out

@@ -312,9 +312,34 @@ def pin_cache_append(orc):
         raise AssertionError("a slot past the pool was accepted")
 
 
+def pin_top_k_renorm(orc):
+    """Top-k renormalisation against closed forms and torch.topk: k = 1 is one-hot at a
+    unique maximum; ties at the pivot are all kept; k <= 0 or k >= V is p / sum p; on rows
+    without ties the kept set is torch.topk's and the kept entries keep their ratios and
+    sum to 1."""
+    p = np.array([[0.1, 0.3, 0.3, 0.3], [0.05, 0.5, 0.2, 0.25], [0.2, 0.2, 0.2, 0.4]])
+    out = orc.top_k_renorm_prob(p, [2, 1, 9])
+    assert np.allclose(out[0], [0, 1 / 3, 1 / 3, 1 / 3], rtol=0, atol=1e-15)
+    assert np.array_equal(out[1], [0, 1, 0, 0])
+    assert np.allclose(out[2], p[2] / p[2].sum(), rtol=0, atol=1e-15)
+    assert np.allclose(orc.top_k_renorm_prob(p, 0), p / p.sum(1, keepdims=True), rtol=0, atol=1e-15)
+    g = torch.Generator().manual_seed(8)
+    logits = torch.randn(6, 5000, generator=g, dtype=torch.float64) * 3
+    probs = torch.softmax(logits, dim=1)
+    ks = [1, 2, 17, 500, 4999, 5000]
+    out = orc.top_k_renorm_prob(probs.numpy(), ks)
+    for r, k in enumerate(ks):
+        keep = np.zeros(5000, dtype=bool)
+        keep[torch.topk(probs[r], min(k, 5000)).indices.numpy()] = True
+        assert np.array_equal(out[r] > 0, keep), (r, k)
+        kept = probs[r].numpy()[keep]
+        assert np.allclose(out[r][keep], kept / kept.sum(), rtol=1e-12, atol=0)
+        assert abs(out[r].sum() - 1.0) < 1e-12
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_bf16, pin_brute_force_sdpa, pin_constant_v, pin_single_key,
     pin_zero_query, pin_duplicate_key, pin_split_merge, pin_merge_weights, pin_permuted_pages,
     pin_head_padding_and_permutation, pin_causal_prefix, pin_sampled_rows, pin_e4m3_encode,
-    pin_cache_append,
+    pin_cache_append, pin_top_k_renorm,
 ]

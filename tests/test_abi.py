@@ -117,3 +117,14 @@ def test_cache_append_rejects_bad_arguments():
     assert call(status=FAKE + 2) == 1
     assert call(n=0, pool=None, x=None, slots=None) == 0  # nothing to do
     assert lib.mla_last_launch_count() == 0
+
+
+def test_top_k_renorm_rejects_bad_arguments():
+    lib = mla.library()
+    assert lib.mla_top_k_renorm_prob(FAKE, FAKE, -1, 10, None, 3, None) == 1
+    assert lib.mla_top_k_renorm_prob(FAKE, FAKE, 2, -5, None, 3, None) == 1
+    assert lib.mla_top_k_renorm_prob(None, FAKE, 2, 10, None, 3, None) == 1
+    assert lib.mla_top_k_renorm_prob(FAKE + 2, FAKE, 2, 10, None, 3, None) == 1
+    assert lib.mla_top_k_renorm_prob(FAKE, FAKE, 2, 10, FAKE + 1, 3, None) == 1
+    assert lib.mla_top_k_renorm_prob(None, None, 0, 10, None, 3, None) == 0  # nothing to do
+    assert lib.mla_last_launch_count() == 0
