@@ -119,6 +119,22 @@ mla_status_t mla_verify(const mla_kv_t* kv, const void* q, int B, int n_q, int H
                         size_t workspace_bytes, void* stream);
 
 /*
+ * mla_verify with a float32 output: the normalised attention output over the keys that kv
+ * describes, not rounded to bfloat16, for results that are merged afterwards. In
+ * decode-context parallelism every rank holds a shard of each sequence's positions, attends
+ * to its shard alone, and the shards' outputs are combined through their log-sum-exp
+ * ("Scaling Kimi K3 on AMD Instinct MI355X: Matching NVIDIA HGX B300 Throughput per GPU on
+ * AgentX", section "缓存可复用，还要能一致地恢复"); keeping the shard outputs in float32
+ * leaves a single bfloat16 rounding, in mla_merge_lse. Arguments, workspace, masking and
+ * errors as mla_verify (workspace from mla_workspace_size(MLA_OP_VERIFY, ...)), except:
+ *   out  device, [B][n_q][H][512] float32 (16-byte aligned)
+ * A sequence with no key gives out = 0 and lse = -inf, which mla_merge_lse weighs as 0.
+ */
+mla_status_t mla_verify_f32(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
+                            float sm_scale, float* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * Causal chunked prefill of one sequence: T new positions attend to the cached prefix
  * and causally to each other ("AMD MI355X推理Kimi K3：吞吐量超NVIDIA，首字优化显著",
  * section "首Token等待优化：简单补零解决大问题": long cold prefill through the MLA

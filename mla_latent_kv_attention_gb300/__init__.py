@@ -29,7 +29,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse",
            "mla_read_status", "mla_status_string", "mla_last_launch_count",
            "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append",
-           "mla_top_k_renorm_prob")
+           "mla_top_k_renorm_prob", "mla_verify_f32")
 
 
 class MlaError(RuntimeError):
@@ -58,6 +58,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_workspace_size.restype = sz
     lib.mla_decode.argtypes = [KV, P, i32, i32, f32, P, P, P, sz, P]
     lib.mla_verify.argtypes = [KV, P, i32, i32, i32, f32, P, P, P, sz, P]
+    lib.mla_verify_f32.argtypes = [KV, P, i32, i32, i32, f32, P, P, P, sz, P]
+    lib.mla_verify_f32.restype = i32
     lib.mla_prefill.argtypes = [KV, P, i32, i32, f32, P, P, P, sz, P]
     lib.mla_merge_lse.argtypes = [P, P, i32, i64, P, P, P]
     lib.mla_read_status.argtypes = [P, sz, P]
@@ -180,6 +182,23 @@ def mla_verify(kv: KVCache, q: torch.Tensor, sm_scale: float, out=None, lse=None
     _check("mla_verify", library().mla_verify(ctypes.byref(c), q.data_ptr(), B, n_q, H, sm_scale,
                                          out.data_ptr(), _ptr(lse), ws.data_ptr(), ws.numel(),
                                          _stream(stream)))
+    return out, lse
+
+
+def mla_verify_f32(kv: KVCache, q: torch.Tensor, sm_scale: float, out=None, lse=None, ws=None,
+                   stream=None):
+    """As mla_verify with a float32 output [B, n_q, H, 512], for results merged later."""
+    _q_check(q, 4)
+    B, n_q, H = q.shape[0], q.shape[1], q.shape[2]
+    out = torch.empty(B, n_q, H, MLA_DV, dtype=torch.float32, device=q.device) if out is None else out
+    if out.dtype != torch.float32 or not out.is_contiguous() or out.shape != (B, n_q, H, MLA_DV):
+        raise ValueError("out must be a contiguous float32 tensor [B, n_q, H, 512]")
+    lse = torch.empty(B, n_q, H, dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(MLA_OP_VERIFY, B, H, n_q, q.device) if ws is None else ws
+    c = kv.c_struct()
+    _check("mla_verify_f32", library().mla_verify_f32(
+        ctypes.byref(c), q.data_ptr(), B, n_q, H, sm_scale, out.data_ptr(), _ptr(lse),
+        ws.data_ptr(), ws.numel(), _stream(stream)))
     return out, lse
 
 

@@ -67,7 +67,8 @@ mla_status_t current_device(int* dev) {
 }
 
 mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H, float sm_scale,
-                       void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+                       void* out, float* lse, void* ws, size_t ws_bytes, void* stream,
+                       bool out_is_f32 = false) {
   g_last_launches = 0;
   mla_status_t st = check_kv(kv);
   if (st != MLA_OK) return st;
@@ -84,6 +85,10 @@ mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
   if (ws_bytes < w.total) return MLA_ERR_WORKSPACE;
   if (B == 0) return MLA_OK;
   mla::AttnParams p = base_params(kv, q, B, n_q, H, sm_scale, out, lse);
+  if (out_is_f32) {
+    p.out = nullptr;
+    p.out_f32 = static_cast<float*>(out);
+  }
   char* base = static_cast<char*>(ws);
   p.hdr = reinterpret_cast<mla::WsHeader*>(base + w.hdr);
   p.status = reinterpret_cast<unsigned*>(base + w.status);
@@ -136,6 +141,12 @@ mla_status_t mla_verify(const mla_kv_t* kv, const void* q, int B, int n_q, int H
                         float sm_scale, void* out, float* lse, void* workspace,
                         size_t workspace_bytes, void* stream) {
   return run_split(kv, q, B, n_q, H, sm_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+mla_status_t mla_verify_f32(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
+                            float sm_scale, float* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return run_split(kv, q, B, n_q, H, sm_scale, out, lse, workspace, workspace_bytes, stream, true);
 }
 
 mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float sm_scale,

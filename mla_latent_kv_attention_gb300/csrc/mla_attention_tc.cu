@@ -187,6 +187,14 @@ __device__ __forceinline__ int seq_len_of(const AttnParams& p, int b) {
 
 __device__ __forceinline__ int blocks_of(int L) { return (L + kKeyBlock - 1) / kKeyBlock; }
 
+// A final output element: bf16, or float32 when the caller asked for it.
+__device__ __forceinline__ void store_out(const AttnParams& p, int64_t idx, float v) {
+  if (p.out_f32)
+    p.out_f32[idx] = v;
+  else
+    p.out[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
 __device__ __forceinline__ Cursor first_unit(const DecodeArgs& a, const Misc* ms) {
   Cursor c;
   c.u = blockIdx.x;
@@ -821,7 +829,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         for (int r = rb; r < rb + RH && r < R; ++r) {
           if (final_out) {
             const int64_t row = (int64_t)un.qrow0 + ms->row_off[r];
-            for (int dv = i; dv < kDV; dv += 128) p.out[row * kDV + dv] = 0;
+            for (int dv = i; dv < kDV; dv += 128) store_out(p, row * kDV + dv, 0.f);
             if (i == 0 && p.lse) p.lse[row] = -INFINITY;
           } else if (i == 0) {
             p.part_lse[(int64_t)un.slot * p.R + ms->row_off[r]] = -INFINITY;
@@ -1036,8 +1044,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           const int dv = c * 128 + i;
           const int roff = ms->row_off[rb + r];
           if (final_out) {
-            p.out[((int64_t)un.qrow0 + roff) * kDV + dv] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv[r]));
+            store_out(p, ((int64_t)un.qrow0 + roff) * kDV + dv, acc * inv[r]);
           } else {
             p.part_out[((int64_t)un.slot * p.R + roff) * kDV + dv] = acc * inv[r];
           }

@@ -100,7 +100,8 @@ struct AttnParams {
   float sm_scale;
   const uint16_t* q;  // [B][n_q][H][576]
   int B, n_q, H, R;   // R = n_q * H rows per sequence
-  uint16_t* out;      // [B][n_q][H][512]
+  uint16_t* out;      // [B][n_q][H][512] bf16
+  float* out_f32;     // when set, the output goes here as float32 instead of to `out`
   float* lse;         // [B][n_q][H] or null
   float* part_out;    // [2 * num_ctas][R][512]
   float* part_lse;    // [2 * num_ctas][R]

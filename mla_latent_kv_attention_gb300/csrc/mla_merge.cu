@@ -29,17 +29,22 @@ constexpr int kMergeThreads = 32 * kMergeWarps;
 // lse values it reduces (every warp reduces them all, no barrier) and warp w's pieces
 // w, w + 8, ..., with their own lse values for the weights; only pieces past the first
 // batch, or lse values past 256, take further rounds. The warps' sums meet in shared memory.
-template <int VEC, typename SlotOf>
+__device__ __forceinline__ void store_val(uint16_t* p, float v) {
+  *p = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ void store_val(float* p, float v) { *p = v; }
+
+template <int VEC, typename OutT, typename SlotOf>
 __device__ void merge_row_chunk(const float* __restrict__ po, const float* __restrict__ pl,
                                 int count, SlotOf slot_of, int64_t r, int64_t R, int chunk,
-                                uint16_t* __restrict__ out_row, float* lse_out) {
+                                OutT* __restrict__ out_row, float* lse_out) {
   constexpr int W = 32 * VEC;                             // dv per CTA
   constexpr int NB = VEC >= 16 ? 2 : (VEC >= 4 ? 8 : 24);  // pieces per batch and warp
   constexpr int kLse = 8;                                 // lse values per lane (256 pieces)
   __shared__ __align__(16) float s_acc[kMergeWarps][W];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (count <= 0) {  // nothing to merge: out = 0, lse = -inf
-    for (int x = threadIdx.x; x < W; x += kMergeThreads) out_row[chunk * W + x] = 0;
+    for (int x = threadIdx.x; x < W; x += kMergeThreads) store_val(out_row + chunk * W + x, 0.f);
     if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
     return;
   }
@@ -134,7 +139,7 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
     float t = 0.f;
 #pragma unroll
     for (int g = 0; g < kMergeWarps; ++g) t += s_acc[g][x];
-    out_row[chunk * W + x] = __bfloat16_as_ushort(__float2bfloat16_rn(t));
+    store_val(out_row + chunk * W + x, t);
   }
   if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = lse;
 }
@@ -142,7 +147,7 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
 // Rows of the decode/verify path whose sequence was split over several CTAs, and rows of
 // sequences with no key at all (out = 0, lse = -inf). Launched as a programmatic dependent
 // of the attention kernel, whose grid it waits for.
-template <int VEC>
+template <int VEC, typename OutT>
 __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = blockIdx.x;  // b * R + r
@@ -151,10 +156,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p
   const int64_t r = row % p.R;
   const SeqSpan sp = p.seqs[b];
   const int64_t total = p.hdr->total_cost, n = p.num_ctas;
-  uint16_t* out_row = p.out + row * kDV;
+  OutT* out_row;
+  if constexpr (sizeof(OutT) == 4)
+    out_row = p.out_f32 + row * kDV;
+  else
+    out_row = p.out + row * kDV;
   float* lse_out = p.lse ? p.lse + row : nullptr;
   if (sp.num_blocks == 0) {
-    for (int x = threadIdx.x; x < 32 * VEC; x += kMergeThreads) out_row[chunk * 32 * VEC + x] = 0;
+    for (int x = threadIdx.x; x < 32 * VEC; x += kMergeThreads)
+      store_val(out_row + chunk * 32 * VEC + x, 0.f);
     if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
     return;
   }
@@ -172,7 +182,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p
     if (i == 0) return 2 * c0 + first_odd;
     return 2 * ((total >= n) ? c0 + i : range_of(pre + i, total, n));
   };
-  merge_row_chunk<VEC>(p.part_out, p.part_lse, count, slot_of, r, p.R, chunk, out_row, lse_out);
+  merge_row_chunk<VEC, OutT>(p.part_out, p.part_lse, count, slot_of, r, p.R, chunk, out_row, lse_out);
 }
 
 template <int VEC>
@@ -180,8 +190,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     merge_standalone_kernel(const float* po, const float* pl, int S, int64_t R, uint16_t* out,
                             float* lse) {
   const int64_t row = blockIdx.x;
-  merge_row_chunk<VEC>(po, pl, S, [](int i) -> int64_t { return i; }, row, R, blockIdx.y,
-                       out + row * kDV, lse ? lse + row : nullptr);
+  merge_row_chunk<VEC, uint16_t>(po, pl, S, [](int i) -> int64_t { return i; }, row, R, blockIdx.y,
+                                 out + row * kDV, lse ? lse + row : nullptr);
 }
 
 // Chunk width: whole 512-wide rows when there are rows enough to fill the GPU, narrower
@@ -206,9 +216,14 @@ cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16>, p);
-  if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4>, p);
-  return cudaLaunchKernelEx(&cfg, merge_split_kernel<1>, p);
+  if (p.out_f32) {
+    if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, float>, p);
+    if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4, float>, p);
+    return cudaLaunchKernelEx(&cfg, merge_split_kernel<1, float>, p);
+  }
+  if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, uint16_t>, p);
+  if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4, uint16_t>, p);
+  return cudaLaunchKernelEx(&cfg, merge_split_kernel<1, uint16_t>, p);
 }
 
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,

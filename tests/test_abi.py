@@ -14,7 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def header_functions():
     src = open(os.path.join(ROOT, "include", "mla.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_what_binding_lists():
@@ -127,4 +127,15 @@ def test_top_k_renorm_rejects_bad_arguments():
     assert lib.mla_top_k_renorm_prob(FAKE + 2, FAKE, 2, 10, None, 3, None) == 1
     assert lib.mla_top_k_renorm_prob(FAKE, FAKE, 2, 10, FAKE + 1, 3, None) == 1
     assert lib.mla_top_k_renorm_prob(None, None, 0, 10, None, 3, None) == 0  # nothing to do
+    assert lib.mla_last_launch_count() == 0
+
+
+def test_verify_f32_rejects_bad_arguments():
+    lib = mla.library()
+    kv = mla.mla_kv_t(FAKE, 4, 64, FAKE, 4, FAKE, 1.0)
+    call = lib.mla_verify_f32
+    assert call(ctypes.byref(kv), FAKE, 1, 5, 12, 1.0, FAKE, FAKE, FAKE, 1 << 20, None) == 2  # n_q > 4
+    assert call(ctypes.byref(kv), FAKE, 1, 1, 0, 1.0, FAKE, FAKE, FAKE, 1 << 20, None) == 2   # H < 1
+    assert call(ctypes.byref(kv), FAKE, 1, 1, 12, 1.0, None, FAKE, FAKE, 1 << 20, None) == 1  # no out
+    assert call(ctypes.byref(kv), FAKE, 1, 1, 12, 1.0, FAKE + 4, FAKE, FAKE, 1 << 20, None) == 1
     assert lib.mla_last_launch_count() == 0

@@ -72,3 +72,27 @@ def test_mutant_is_caught(name):
         finally:
             oracle.use_library(prev)
     assert caught, f"no pin caught mutant {name}"
+
+
+# Mistakes planted in the oracle's Python-level functions (top-k renormalisation).
+PY_MUTANTS = {
+    "topk_drops_ties": ("keep = p[r] >= pivot", "keep = p[r] > pivot"),
+    "topk_off_by_one_pivot": ("pivot = np.sort(p[r])[V - k]", "pivot = np.sort(p[r])[V - k - 1]"),
+    "topk_renorm_by_row_sum": ("out[r, keep] = p[r, keep] / p[r, keep].sum()",
+                               "out[r, keep] = p[r, keep] / p[r].sum()"),
+    "topk_keep_all_at_v_minus_1": ("if k <= 0 or k >= V:", "if k <= 0 or k >= V - 1:"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_py_mutant_is_caught(name):
+    import inspect
+    import types
+    old, new = PY_MUTANTS[name]
+    src = inspect.getsource(oracle.top_k_renorm_prob)
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    shim = types.SimpleNamespace(top_k_renorm_prob=ns["top_k_renorm_prob"])
+    with pytest.raises(AssertionError):
+        oracle_pins.pin_top_k_renorm(shim)
