@@ -2,6 +2,8 @@
 
     python -m mla_latent_kv_attention_gb300.run_workload batched_paged_decode --iters 5
     python -m mla_latent_kv_attention_gb300.run_workload causal_prefill --T 2048 --iters 3
+    python -m mla_latent_kv_attention_gb300.run_workload cache_append --iters 5
+    python -m mla_latent_kv_attention_gb300.run_workload top_k_renorm --iters 5
 
 Prints the device status word after the last call. Intended as the command line that
 ncu wraps: every launch it makes is a library launch on the named inputs.
@@ -19,11 +21,15 @@ from mla_latent_kv_attention_gb300 import workloads as W
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("workload", choices=sorted(W.WORKLOADS))
+    ap.add_argument("workload", choices=sorted(W.WORKLOADS) + ["cache_append", "top_k_renorm"])
     ap.add_argument("--iters", type=int, default=5)
     ap.add_argument("--heads", type=int, default=12, help="long_history_decode only")
     ap.add_argument("--T", type=int, default=8192, help="causal_prefill only")
     args = ap.parse_args(argv)
+    if args.workload == "cache_append":
+        return _cache_append(args.iters)
+    if args.workload == "top_k_renorm":
+        return _top_k_renorm(args.iters)
     if args.workload == "long_history_decode":
         inp = W.long_history_decode(args.heads)
     elif args.workload == "causal_prefill":
@@ -48,6 +54,36 @@ def main(argv=None) -> int:
     status = mla.mla_read_status(ws)
     print(f"{args.workload}: {args.iters} calls, status {mla.STATUS.get(status, status)}")
     return 0 if status == 0 else 1
+
+
+def _cache_append(iters: int) -> int:
+    """8,192 bf16 rows (a prefill chunk) into a 302 MB pool of 64-position pages at random
+    slots, a different slot set each call."""
+    g = torch.Generator().manual_seed(7)
+    pool = torch.zeros(8192, 64, mla.MLA_D, dtype=torch.uint8, device="cuda")
+    x = torch.randn(8192, mla.MLA_D, generator=g).to(torch.bfloat16).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for i in range(iters):
+        slots = torch.randperm(pool.shape[0] * 64, generator=g)[:8192].cuda()
+        mla.mla_cache_append(pool, x, slots, 0.0125, status=status)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    print(f"cache_append: {iters} calls, status {mla.STATUS.get(st, st)}")
+    return 0 if st == 0 else 1
+
+
+def _top_k_renorm(iters: int) -> int:
+    """32 probability rows over a 129,280-entry vocabulary, k drawn per row in [1, 1024)."""
+    g = torch.Generator().manual_seed(1)
+    probs = torch.softmax(torch.randn(32, 129280, generator=g) * 3, dim=1).cuda()
+    ks = torch.randint(1, 1024, (32,), generator=g, dtype=torch.int32).cuda()
+    out = torch.empty_like(probs)
+    for _ in range(iters):
+        mla.mla_top_k_renorm_prob(probs, ks, out=out)
+    torch.cuda.synchronize()
+    ok = bool(torch.isfinite(out).all().item())
+    print(f"top_k_renorm: {iters} calls, {'finite' if ok else 'NON-FINITE'} output")
+    return 0 if ok else 1
 
 
 if __name__ == "__main__":

@@ -190,6 +190,56 @@ def causal_prefill(T: int = 8192, prefix: int = 32768, H: int = 12, seed: int = 
     return make_inputs(f"causal_prefill_t{T}_p{prefix}_h{H}", [prefix + T], H=H, n_q=T, seed=seed)
 
 
+@dataclasses.dataclass
+class MhaInputs:
+    """One MHA-form (non-absorbed) prefill workload of one sequence, all on the CPU.
+
+    cache   MlaInputs with B = 1 and n_q = T: the paged latent cache (its absorbed q is
+            not used by the MHA form)
+    q       bfloat16 [T][H][192]   per head: 128 no-RoPE dims, then the 64 RoPE dims
+    w_ukv   bfloat16 [512][H][256] per head: W_UK (columns 0..127) then W_UV (128..255);
+            key h of position n = [latent_n @ W_UK_h ; rope_n], value = latent_n @ W_UV_h
+    """
+
+    cache: MlaInputs
+    q: torch.Tensor
+    w_ukv: torch.Tensor
+
+    @property
+    def T(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def H(self) -> int:
+        return int(self.q.shape[1])
+
+
+QK_NOPE = 128  # up-projected key dims per head
+QK_ROPE = 64   # RoPE dims (shared by the heads)
+V_HEAD = 128   # up-projected value dims per head
+
+
+def mha_prefill_inputs(T: int, prefix: int, H: int = 12, seed: int = 0,
+                       page_size: int = PAGE) -> MhaInputs:
+    """The cache as ``make_inputs`` draws it (one sequence of prefix + T positions), then,
+    from a second generator seeded ``seed + 1``: q ~ N(0, 1) [T][H][192] and
+    w_ukv ~ N(0, 1/512) [512][H][256] (so up-projected keys and values have unit variance
+    like the RoPE part), each rounded to bfloat16. The pages give no weights; these are
+    synthetic stand-ins."""
+    cache = make_inputs(f"mha_prefill_t{T}_p{prefix}_h{H}", [prefix + T], H=H, n_q=T,
+                        page_size=page_size, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn(T, H, QK_NOPE + QK_ROPE, generator=g).to(torch.bfloat16)
+    w = (torch.randn(DV, H, QK_NOPE + V_HEAD, generator=g) / math.sqrt(DV)).to(torch.bfloat16)
+    return MhaInputs(cache=cache, q=q, w_ukv=w)
+
+
+def mha_prefill(T: int = 8192, prefix: int = 32768, H: int = 12, seed: int = 0) -> MhaInputs:
+    """The causal prefill chunk of the named workload (T new positions on a prefix) in the
+    MHA form."""
+    return mha_prefill_inputs(T, prefix, H, seed)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "batched_paged_decode": batched_paged_decode,

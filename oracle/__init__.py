@@ -214,3 +214,60 @@ def top_k_renorm_prob(probs, top_k):
             keep = p[r] >= pivot
         out[r, keep] = p[r, keep] / p[r, keep].sum()
     return out
+
+
+def _cache_rows(cache, L: int) -> np.ndarray:
+    """Dequantised rows 0..L-1 of sequence 0 of an MlaInputs cache, float64 [L][576]."""
+    table = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64) * float(cache.kv_scale)
+    pool = _np(cache.pool, np.uint8)
+    pt = _np(cache.page_table, np.int32)
+    P = pool.shape[1]
+    n = np.arange(L)
+    pages = pt[0, n // P]
+    if (pages < 0).any() or (pages >= pool.shape[0]).any():
+        raise ValueError("page index outside the pool")
+    return table[pool[pages, n % P]]
+
+
+def _f64(t) -> np.ndarray:
+    if hasattr(t, "detach"):
+        return t.detach().cpu().double().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def mha_prefill_rows(cache, q, w_ukv, rows=None):
+    """MHA-form causal prefill of one sequence in float64, from the definition: for head h
+    the key of position n is [c_n W_UK_h ; r_n] (c_n the 512-wide latent, r_n the 64 RoPE
+    dims, both dequantised), its value c_n W_UV_h; new position t (of T, the last T of the
+    L cached) sees keys n <= L - T + t; scores are scaled by sm_scale.
+    q [T][H][192], w_ukv [512][H][256] (W_UK_h = columns 0..127, W_UV_h = 128..255).
+    rows: None for every (t, h), else an int array [n, 2] of (t, h).
+    Returns (out [T][H][128] or [n][128], lse [T][H] or [n])."""
+    qf = _f64(q)
+    W = _f64(w_ukv)
+    T, H = qf.shape[0], qf.shape[1]
+    L = int(_np(cache.seq_lens, np.int32)[0])
+    if L < T:
+        raise ValueError("the sequence must hold its T new positions")
+    kv = _cache_rows(cache, L)
+    c, r = kv[:, :DV], kv[:, DV:]
+    sel = np.array([(t, h) for t in range(T) for h in range(H)]) if rows is None else \
+        np.asarray(rows, dtype=np.int64).reshape(-1, 2)
+    out = np.zeros((sel.shape[0], 128))
+    lse = np.full((sel.shape[0],), -np.inf)
+    for h in np.unique(sel[:, 1]):
+        K = np.concatenate([c @ W[:, h, :128], r], axis=1)   # [L][192]
+        V = c @ W[:, h, 128:]                                # [L][128]
+        idx = np.nonzero(sel[:, 1] == h)[0]
+        ts = sel[idx, 0]
+        s = float(cache.sm_scale) * (qf[ts, h, :] @ K.T)     # [n][L]
+        visible = np.arange(L)[None, :] <= (L - T + ts)[:, None]
+        s = np.where(visible, s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        l = p.sum(axis=1, keepdims=True)
+        out[idx] = (p @ V) / l
+        lse[idx] = (m + np.log(l))[:, 0]
+    if rows is None:
+        return out.reshape(T, H, 128), lse.reshape(T, H)
+    return out, lse

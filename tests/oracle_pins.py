@@ -337,9 +337,98 @@ def pin_top_k_renorm(orc):
         assert abs(out[r].sum() - 1.0) < 1e-12
 
 
+def _selection(rng, H, n_out):
+    """Per head: distinct rows of the 512-wide latent and signs, as a [512][H][n_out] matrix
+    with one +-1 per column."""
+    w = np.zeros((512, H, n_out))
+    picks = []
+    for h in range(H):
+        rows = rng.permutation(512)[:n_out]
+        signs = rng.choice([-1.0, 1.0], n_out)
+        w[rows, h, np.arange(n_out)] = signs
+        picks.append((rows, signs))
+    return w, picks
+
+
+def pin_mha_absorbed_identity(orc):
+    """The MHA form and the absorbed form are one computation ("MI355X Kimi K2.5 vLLM AITER
+    7x speedup", section "PR #35850 修复了什么": keys and values come from one shared latent):
+    with W_UK_h and W_UV_h signed selections, the absorbed query [W_UK_h q_nope ; q_rope] is
+    exact in bf16, the absorbed oracle's scores equal the MHA scores, and the MHA output is
+    the selected, signed entries of the absorbed output."""
+    rng = np.random.default_rng(21)
+    T, H = 5, 3
+    m = W.mha_prefill_inputs(T, 120, H=H, seed=21)
+    wk, pk = _selection(rng, H, 128)
+    wv, pv = _selection(rng, H, 128)
+    w = torch.from_numpy(np.concatenate([wk, wv], axis=2)).to(torch.bfloat16)
+    out, lse = orc.mha_prefill_rows(m.cache, m.q, w)
+    qf = m.q.double().numpy()
+    q_abs = np.zeros((1, T, H, 576))
+    for h in range(H):
+        rows, signs = pk[h]
+        q_abs[0, :, h, rows] = (qf[:, h, :128] * signs).T
+        q_abs[0, :, h, 512:] = qf[:, h, 128:]
+    qa = torch.from_numpy(q_abs).to(torch.bfloat16)
+    assert np.array_equal(qa.double().numpy(), q_abs)  # exact in bf16
+    absorbed = W.MlaInputs("abs", m.cache.pool, m.cache.page_table, m.cache.seq_lens, qa,
+                           m.cache.kv_scale, m.cache.sm_scale, m.cache.page_size)
+    out_a, lse_a = orc.attention(absorbed)
+    for h in range(H):
+        rows, signs = pv[h]
+        np.testing.assert_allclose(out[:, h], out_a[0, :, h][:, rows] * signs, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_a[0], rtol=1e-12)
+
+
+def pin_mha_zero_query(orc):
+    """q = 0: every visible key weighs the same, so out = the mean of the visible values and
+    lse = ln(#visible); position t of T sees L - T + t + 1 keys."""
+    m = W.mha_prefill_inputs(4, 37, H=2, seed=22)
+    q0 = torch.zeros_like(m.q)
+    out, lse = orc.mha_prefill_rows(m.cache, q0, m.w_ukv)
+    L, T = 41, 4
+    kv = np.zeros((L, 576))
+    table = np.array([orc.e4m3_value(c) for c in range(256)]) * m.cache.kv_scale
+    pt = m.cache.page_table[0].numpy()
+    P = m.cache.page_size
+    for n in range(L):
+        kv[n] = table[m.cache.pool[pt[n // P], n % P].numpy()]
+    Wf = m.w_ukv.double().numpy()
+    for t in range(T):
+        vis = L - T + t + 1
+        for h in range(2):
+            v = kv[:vis, :512] @ Wf[:, h, 128:]
+            np.testing.assert_allclose(out[t, h], v.mean(axis=0), rtol=1e-10, atol=1e-13)
+            assert abs(lse[t, h] - math.log(vis)) < 1e-12
+
+
+def pin_mha_sdpa(orc):
+    """Against torch's float64 scaled_dot_product_attention with an explicit bottom-right
+    causal mask, on keys and values built with torch (einsum) from the same codes."""
+    m = W.mha_prefill_inputs(6, 90, H=3, seed=23)
+    out, lse = orc.mha_prefill_rows(m.cache, m.q, m.w_ukv)
+    L, T, H = 96, 6, 3
+    codes = torch.stack([m.cache.pool[m.cache.page_table[0, n // 64], n % 64] for n in range(L)])
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64) * m.cache.kv_scale
+    Wf = m.w_ukv.double()
+    K = torch.cat([torch.einsum("nd,dhk->hnk", vals[:, :512], Wf[:, :, :128]),
+                   vals[None, :, 512:].expand(H, L, 64)], dim=2)
+    V = torch.einsum("nd,dhk->hnk", vals[:, :512], Wf[:, :, 128:])
+    q = m.q.double().permute(1, 0, 2)
+    mask = torch.arange(L)[None, :] <= (L - T + torch.arange(T))[:, None]
+    ref = F.scaled_dot_product_attention(q, K, V, attn_mask=mask, scale=m.cache.sm_scale)
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+    rows = np.array([[5, 2], [0, 0], [3, 1]])
+    o, l = orc.mha_prefill_rows(m.cache, m.q, m.w_ukv, rows)
+    for i, (t, h) in enumerate(rows):  # (BLAS may block a different row count differently)
+        np.testing.assert_allclose(o[i], out[t, h], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(l[i], lse[t, h], rtol=1e-14)
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_bf16, pin_brute_force_sdpa, pin_constant_v, pin_single_key,
     pin_zero_query, pin_duplicate_key, pin_split_merge, pin_merge_weights, pin_permuted_pages,
     pin_head_padding_and_permutation, pin_causal_prefix, pin_sampled_rows, pin_e4m3_encode,
-    pin_cache_append, pin_top_k_renorm,
+    pin_cache_append, pin_top_k_renorm, pin_mha_absorbed_identity, pin_mha_zero_query,
+    pin_mha_sdpa,
 ]

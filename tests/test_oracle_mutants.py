@@ -96,3 +96,36 @@ def test_py_mutant_is_caught(name):
     shim = types.SimpleNamespace(top_k_renorm_prob=ns["top_k_renorm_prob"])
     with pytest.raises(AssertionError):
         oracle_pins.pin_top_k_renorm(shim)
+
+
+# Mistakes planted in the MHA-form prefill oracle.
+MHA_MUTANTS = {
+    "mha_drops_rope": ("K = np.concatenate([c @ W[:, h, :128], r], axis=1)",
+                       "K = np.concatenate([c @ W[:, h, :128], 0 * r], axis=1)"),
+    "mha_uk_uv_swapped": ("V = c @ W[:, h, 128:]", "V = c @ W[:, h, :128]"),
+    "mha_causal_off_by_one": ("<= (L - T + ts)[:, None]", "< (L - T + ts)[:, None]"),
+    "mha_head_of_weights": ("K = np.concatenate([c @ W[:, h, :128], r], axis=1)",
+                            "K = np.concatenate([c @ W[:, 0, :128], r], axis=1)"),
+    "mha_no_scale": ("s = float(cache.sm_scale) * (qf[ts, h, :] @ K.T)", "s = qf[ts, h, :] @ K.T"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MHA_MUTANTS))
+def test_mha_mutant_is_caught(name):
+    import inspect
+    import types
+    old, new = MHA_MUTANTS[name]
+    src = inspect.getsource(oracle.mha_prefill_rows)
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    shim = types.SimpleNamespace(**{k: getattr(oracle, k) for k in ("attention", "e4m3_value")},
+                                 mha_prefill_rows=ns["mha_prefill_rows"])
+    caught = []
+    for pin in (oracle_pins.pin_mha_absorbed_identity, oracle_pins.pin_mha_zero_query,
+                oracle_pins.pin_mha_sdpa):
+        try:
+            pin(shim)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutant {name}"
