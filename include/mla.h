@@ -148,6 +148,34 @@ mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float 
                          void* stream);
 
 /*
+ * Causal prefill of one sequence in the MHA (non-absorbed) form. Keys and values of every
+ * head are up-projected from the shared latent ("MI355X Kimi K2.5 vLLM AITER 7x speedup",
+ * section "PR #35850 修复了什么": K and V come from one compressed latent): for head h and
+ * cached position n, key = [c_n W_UK_h ; r_n] (192 wide) and value = c_n W_UV_h (128 wide),
+ * c_n the 512-wide latent and r_n the 64 RoPE dims of the row, dequantised under
+ * kv->kv_scale. New position t (of the last T of L cached) sees keys n <= L - T + t; scores
+ * are q . key x sm_scale. The up-projected keys and values are bfloat16, and so are the
+ * probabilities that meet the values (tensor-core operands), so results carry a few more
+ * bf16 roundings than mla_prefill.
+ *   kv     the cache (page size a multiple of 64); kv->seq_lens is not read: L is given
+ *          on the host because it sizes the up-projection; sequence 0 of the page table
+ *   L      cached positions including the T new ones, 1 <= T <= L <= page-table capacity
+ *   q      device, [T][H][192] bfloat16 (128 no-RoPE dims, then 64 RoPE dims), 16-B aligned
+ *   w_ukv  device, [512][H][256] bfloat16: for head h, columns 0..127 are W_UK_h and
+ *          128..255 are W_UV_h
+ *   out    device, [T][H][128] bfloat16, 16-B aligned
+ *   lse    device, [T][H] float32 (natural log), or NULL
+ *   workspace  device, 256-B aligned, mla_prefill_mha_workspace_size(L, H, device) bytes:
+ *          the dequantised latent, the up-projected keys and values, status words.
+ * Errors as mla_prefill; a page index outside the pool is reported by mla_read_status.
+ * Launches: a dequantisation kernel, one cuBLAS GEMM, the attention kernel.
+ */
+size_t mla_prefill_mha_workspace_size(int L, int H, int device);
+mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, int H,
+                             const void* w_ukv, float sm_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Log-sum-exp merge of S partial results per row ("Scaling Kimi K3 ...", section
  * "缓存可复用，还要能一致地恢复"): lse = ln sum_s exp(lse_s),
  * out = sum_s exp(lse_s - lse) * out_s. Partials with lse_s = -inf carry weight 0; a row

@@ -29,7 +29,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla_merge_lse",
            "mla_read_status", "mla_status_string", "mla_last_launch_count",
            "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append",
-           "mla_top_k_renorm_prob", "mla_verify_f32")
+           "mla_top_k_renorm_prob", "mla_verify_f32", "mla_prefill_mha",
+           "mla_prefill_mha_workspace_size")
 
 
 class MlaError(RuntimeError):
@@ -60,6 +61,10 @@ def _load() -> ctypes.CDLL:
     lib.mla_verify.argtypes = [KV, P, i32, i32, i32, f32, P, P, P, sz, P]
     lib.mla_verify_f32.argtypes = [KV, P, i32, i32, i32, f32, P, P, P, sz, P]
     lib.mla_verify_f32.restype = i32
+    lib.mla_prefill_mha_workspace_size.argtypes = [i32, i32, i32]
+    lib.mla_prefill_mha_workspace_size.restype = sz
+    lib.mla_prefill_mha.argtypes = [KV, i32, P, i32, i32, P, f32, P, P, P, sz, P]
+    lib.mla_prefill_mha.restype = i32
     lib.mla_prefill.argtypes = [KV, P, i32, i32, f32, P, P, P, sz, P]
     lib.mla_merge_lse.argtypes = [P, P, i32, i64, P, P, P]
     lib.mla_read_status.argtypes = [P, sz, P]
@@ -182,6 +187,32 @@ def mla_verify(kv: KVCache, q: torch.Tensor, sm_scale: float, out=None, lse=None
     _check("mla_verify", library().mla_verify(ctypes.byref(c), q.data_ptr(), B, n_q, H, sm_scale,
                                          out.data_ptr(), _ptr(lse), ws.data_ptr(), ws.numel(),
                                          _stream(stream)))
+    return out, lse
+
+
+def mla_prefill_mha(kv: KVCache, q: torch.Tensor, w_ukv: torch.Tensor, sm_scale: float,
+                    L: Optional[int] = None, out=None, lse=None, ws=None, stream=None):
+    """MHA-form causal prefill of sequence 0: q [T, H, 192] bf16, w_ukv [512, H, 256] bf16
+    -> (out [T, H, 128] bf16, lse [T, H] fp32). L (cached positions incl. the T new ones)
+    defaults to kv.seq_lens[0]."""
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != 192 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bfloat16 tensor [T, H, 192]")
+    T, H = q.shape[0], q.shape[1]
+    if w_ukv.dtype != torch.bfloat16 or tuple(w_ukv.shape) != (512, H, 256) or not w_ukv.is_contiguous():
+        raise ValueError("w_ukv must be a contiguous bfloat16 tensor [512, H, 256]")
+    if L is None:
+        L = int(kv.seq_lens[0].item())
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty(T, H, dtype=torch.float32, device=q.device) if lse is None else lse
+    if ws is None:
+        n = int(library().mla_prefill_mha_workspace_size(L, H, q.device.index or 0))
+        if n == 0:
+            raise ValueError("no workspace size for these arguments")
+        ws = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    c = kv.c_struct()
+    _check("mla_prefill_mha", library().mla_prefill_mha(
+        ctypes.byref(c), L, q.data_ptr(), T, H, w_ukv.data_ptr(), sm_scale, out.data_ptr(),
+        _ptr(lse), ws.data_ptr(), ws.numel(), _stream(stream)))
     return out, lse
 
 

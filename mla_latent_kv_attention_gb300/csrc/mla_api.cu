@@ -149,6 +149,68 @@ mla_status_t mla_verify_f32(const mla_kv_t* kv, const void* q, int B, int n_q, i
   return run_split(kv, q, B, n_q, H, sm_scale, out, lse, workspace, workspace_bytes, stream, true);
 }
 
+size_t mla_prefill_mha_workspace_size(int L, int H, int device) {
+  if (L < 0 || H < 1 || H > MLA_MAX_HEADS) return 0;
+  const int sms = sm_count(device);
+  if (sms <= 0) return 0;
+  return mla::mha_ws_layout(L, H, sms).total;
+}
+
+mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, int H,
+                             const void* w_ukv, float sm_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  mla_status_t st = check_kv(kv);
+  if (st != MLA_OK) return st;
+  if (T < 0 || L < T) return MLA_ERR_INVALID_ARG;
+  if (H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_UNSUPPORTED;
+  if (!q || !w_ukv || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(w_ukv, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
+    return MLA_ERR_INVALID_ARG;
+  if ((int64_t)L > kv->page_table_stride * (int64_t)kv->page_size) return MLA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+  if (workspace_bytes < sizeof(mla::WsHeader)) return MLA_ERR_WORKSPACE;
+  if (T == 0) return MLA_OK;
+  int dev;
+  if ((st = current_device(&dev)) != MLA_OK) return st;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const mla::MhaWsLayout w = mla::mha_ws_layout(L, H, sms);
+  if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  mla::MhaArgs a;
+  a.pool = kv->pool;
+  a.num_pages = kv->num_pages;
+  a.page_size = kv->page_size;
+  a.page_table = kv->page_table;
+  a.kv_scale = kv->kv_scale;
+  a.L = L;
+  a.T = T;
+  a.H = H;
+  a.sm_scale = sm_scale;
+  a.q = q;
+  a.w_ukv = w_ukv;
+  a.latent = base + w.latent;
+  a.rope = base + w.rope;
+  a.kvup = base + w.kvup;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.status = reinterpret_cast<unsigned*>(base + w.status);
+  a.hdr = reinterpret_cast<mla::WsHeader*>(base);
+  a.device = dev;
+  a.prof_start = g_prof_start;  // the profiling events bracket the attention kernel alone
+  a.prof_stop = g_prof_stop;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launched = 0;
+  const cudaError_t e = mla::launch_mha_prefill(a, sms, s, &launched);
+  g_last_launches += launched;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
 mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float sm_scale,
                          void* out, float* lse, void* workspace, size_t workspace_bytes,
                          void* stream) {

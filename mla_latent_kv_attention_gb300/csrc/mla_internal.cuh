@@ -122,6 +122,48 @@ __host__ __device__ __forceinline__ int64_t range_of(int64_t x, int64_t total, i
   return ((x + 1) * n + total - 1) / total - 1;
 }
 
+// MHA-form prefill workspace: header, status words (one per attention CTA, then one for the
+// dequantisation), the dequantised latent [L][512] bf16, the RoPE rows [L][64] bf16 and the
+// up-projected keys and values [L][H][256] bf16 (per head 128 key dims, then 128 value dims).
+struct MhaWsLayout {
+  size_t status, latent, rope, kvup, total;
+};
+inline MhaWsLayout mha_ws_layout(int64_t L, int H, int num_sms) {
+  MhaWsLayout w;
+  size_t off = align_up(sizeof(WsHeader), 256);
+  w.status = off;
+  off = align_up(off + sizeof(unsigned) * (size_t)(num_sms + 1), 256);
+  w.latent = off;
+  off = align_up(off + (size_t)L * kDV * 2, 256);
+  w.rope = off;
+  off = align_up(off + (size_t)L * 64 * 2, 256);
+  w.kvup = off;
+  off = align_up(off + (size_t)L * H * 256 * 2, 256);
+  w.total = off;
+  return w;
+}
+
+struct MhaArgs {
+  const uint8_t* pool;
+  int64_t num_pages;
+  int page_size;
+  const int32_t* page_table;
+  float kv_scale;
+  int L, T, H;
+  float sm_scale;
+  const void* q;      // [T][H][192] bf16
+  const void* w_ukv;  // [512][H][256] bf16
+  void* latent;
+  void* rope;
+  void* kvup;
+  uint16_t* out;      // [T][H][128] bf16
+  float* lse;         // [T][H] or null
+  unsigned* status;   // [num attention CTAs + 1]
+  WsHeader* hdr;
+  int device;
+  cudaEvent_t prof_start, prof_stop;  // recorded around the attention kernel when both set
+};
+
 // Launchers (each returns the CUDA error of its launch).
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
@@ -131,6 +173,7 @@ cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse
 cudaError_t launch_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t* x,
                                 const int64_t* slots, int64_t n, float inv, unsigned* status,
                                 int num_sms, cudaStream_t s);
+cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_top_k_renorm(const float* probs, float* out, int B, int V, const int32_t* top_k,
                                 int k_all, cudaStream_t s);
 

@@ -1,0 +1,546 @@
+// mla_mha_prefill.cu -- causal prefill of one sequence in the MHA (non-absorbed) form.
+//
+// Keys and values of every head come from the one shared latent ("MI355X Kimi K2.5 vLLM
+// AITER 7x speedup", section "PR #35850 修复了什么"): key_h(n) = [c_n W_UK_h ; r_n] (192
+// wide: 128 up-projected dims, then the 64 RoPE dims every head shares), value_h(n) =
+// c_n W_UV_h (128 wide), with c_n the 512-wide latent and r_n the RoPE part of cached row n,
+// both dequantised from e4m3 under kv_scale. New position t of the T (the last T of the L
+// cached) attends causally: keys n <= L - T + t. In this form the attention costs
+// 2 x (192 + 128) flops per (query, key, head) instead of 2 x (576 + 512), at the price of
+// one up-projection GEMM over the cached rows.
+//
+// Three steps:
+//   1. mha_dequant_kernel: cached rows -> latent [L][512] bf16 (e4m3 values, exact; the
+//      scale goes into the GEMM) and RoPE rows [L][64] bf16 (scaled).
+//   2. cuBLAS GEMM (a plain library GEMM): kvup [L][H][256] = kv_scale * latent @ W_ukv.
+//   3. mha_attn_kernel: flash attention on tcgen05. One persistent CTA per SM walks units
+//      of (128 new positions, one head), longest first. Per 128-key tile: S = Q K^T
+//      (M = 128 queries, N = 128 keys, K = 192; twelve kind::f16 MMAs) into one of two TMEM
+//      score buffers; two softmax warpgroups (64 keys each) turn S into bf16 probabilities
+//      written back over the scores they came from; O += P V with P read from TMEM
+//      (A operand) and V from shared memory (MN-major). Lazy rescale: O is rescaled only
+//      when a row's maximum grows by more than 2^8.
+#include <cublas_v2.h>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "mla_internal.cuh"
+#include "sm100.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;                       // new positions per unit
+constexpr int kBN = 128;                       // keys per tile
+constexpr int kBox = 128 * 128;                // one 64-wide bf16 box of 128 rows (16 KB)
+constexpr int kQBytes = 3 * kBox;              // q: dims 0..63, 64..127, 128..191
+constexpr int kKBytes = 3 * kBox;              // keys: two up-projected boxes, then RoPE
+constexpr int kVBytes = 2 * kBox;              // values: dims 0..63, 64..127
+constexpr int kStageBytes = kKBytes + kVBytes;  // 80 KB
+constexpr int kStages = 2;
+constexpr int kThreads = 384;                  // warp 0 TMA, 1 MMA, 4..11 softmax
+constexpr uint32_t kTmemCols = 512;            // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kColO = 256;
+constexpr int kOffStages = kQBytes;
+constexpr int kOffMisc = kQBytes + kStages * kStageBytes;
+constexpr uint64_t kWaitNs = 1000000000ull;    // every wait gives up after 1 s
+constexpr float kRescale = 8.f;                // log2 growth of a row maximum that forces a rescale
+
+struct Misc {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t q_full, q_free;
+  uint64_t pair_bar;  // bounded barrier of the two softmax warpgroups (256 arrivals)
+  uint32_t tmem_base;
+  int abort;
+  unsigned status;
+  float red_max[2][2][kBM];  // [tile parity][warpgroup][row]
+  float red_sum[2][kBM];
+};
+
+constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+// 2^x on the SFU (the PTX instruction; inputs are <= 0 or -inf here)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct MhaParams {
+  int L, T, H;
+  float scale_log2;  // sm_scale * log2(e)
+  uint16_t* out;     // [T][H][128]
+  float* lse;        // [T][H] or null
+  unsigned* status;  // [gridDim.x]
+  WsHeader* hdr;
+};
+
+__device__ __forceinline__ void report(Misc* m, mla_status_t code) {
+  atomicCAS(&m->status, 0u, (unsigned)code);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Misc* m) {
+  if (mbar_wait(bar, parity, kWaitNs)) return true;
+  m->abort = 1;
+  report(m, MLA_ERR_TIMEOUT);
+  return false;
+}
+
+// Units: (query tile, head), ordered longest first (the last query tile sees the most keys),
+// dealt to the CTAs in a snake: round r gives unit r*G + c to CTA c for even r and to CTA
+// G-1-c for odd r.
+struct Unit {
+  int q0, h, ntiles;
+};
+
+__device__ __forceinline__ int num_qtiles(const MhaParams& p) { return (p.T + kBM - 1) / kBM; }
+
+__device__ __forceinline__ Unit unit_at(const MhaParams& p, int u) {
+  const int nq = num_qtiles(p);
+  Unit x;
+  const int qt = nq - 1 - u / p.H;
+  x.h = u % p.H;
+  x.q0 = qt * kBM;
+  const int last = min(x.q0 + kBM, p.T) - 1;      // last new position of the tile
+  const int keys = p.L - p.T + last + 1;           // keys the last position sees
+  x.ntiles = (keys + kBN - 1) / kBN;
+  return x;
+}
+
+__device__ __forceinline__ int unit_of(int r, int c, int G) {
+  return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mha_attn_kernel(const MhaParams p, const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_kv,
+                    const __grid_constant__ CUtensorMap map_rope) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Misc* ms = reinterpret_cast<Misc*>(smem + kOffMisc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int U = num_qtiles(p) * p.H;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ms->full[s], 1);
+      mbar_init(&ms->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->s_full[i], 1);
+      mbar_init(&ms->p_full[i], 256);
+      mbar_init(&ms->pv_done[i], 1);
+    }
+    mbar_init(&ms->q_full, 1);
+    mbar_init(&ms->q_free, 1);
+    mbar_init(&ms->pair_bar, 256);
+    ms->abort = 0;
+    ms->status = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&map_q);
+    prefetch_tensormap(&map_kv);
+    prefetch_tensormap(&map_rope);
+    if (c == 0) p.hdr->num_ctas = G + 1;  // + the dequantisation's status word
+  }
+  if (warp == 1) tmem_alloc(&ms->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms->tmem_base;
+
+  if (warp == 0) {
+    // ---- TMA producer ----
+    if (lane == 0) {
+      int g = 0, k = 0;
+      for (int r = 0;; ++r) {
+        const int u = unit_of(r, c, G);
+        if (u >= U || ms->abort) break;
+        const Unit x = unit_at(p, u);
+        if (k > 0 && !wait_or_abort(&ms->q_free, (k - 1) & 1, ms)) break;
+        mbar_arrive_expect_tx(&ms->q_full, kQBytes);
+        for (int b = 0; b < 3; ++b) tma_load_3d(smem + b * kBox, &map_q, 64 * b, x.h, x.q0, &ms->q_full);
+        bool ok = true;
+        for (int j = 0; j < x.ntiles; ++j, ++g) {
+          const int s = g & 1;
+          if (g >= 2 && !(ok = wait_or_abort(&ms->empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
+          uint8_t* st = smem + kOffStages + s * kStageBytes;
+          mbar_arrive_expect_tx(&ms->full[s], kStageBytes);
+          const int n0 = j * kBN;
+          tma_load_3d(st, &map_kv, 0, x.h, n0, &ms->full[s]);
+          tma_load_3d(st + kBox, &map_kv, 64, x.h, n0, &ms->full[s]);
+          tma_load_2d(st + 2 * kBox, &map_rope, 0, n0, &ms->full[s]);
+          tma_load_3d(st + kKBytes, &map_kv, 128, x.h, n0, &ms->full[s]);
+          tma_load_3d(st + kKBytes + kBox, &map_kv, 192, x.h, n0, &ms->full[s]);
+        }
+        if (!ok) break;
+        ++k;
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = instr_desc(1, 1, 0, 0, 128, 128);  // bf16, both K-major
+      constexpr uint32_t idesc_pv = instr_desc(1, 1, 0, 1, 128, 128);  // P from TMEM, V MN-major
+      const uint32_t q_addr = smem_addr(smem);
+      const uint32_t st_addr = smem_addr(smem + kOffStages);
+      auto pv = [&](int gx, bool first) -> bool {
+        if (!wait_or_abort(&ms->p_full[gx & 1], (gx >> 1) & 1, ms)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = st_addr + (gx & 1) * kStageBytes + kKBytes;
+        const uint32_t pcol = tmem + (gx & 1) * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t a = pcol + (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
+          const uint64_t b = smem_desc(v_addr + ks * 2048, kBox, 1024, Swizzle::k128B);
+          mma_f16_tmem_a(tmem + kColO, a, b, idesc_pv, (first && ks == 0) ? 0u : 1u);
+        }
+        mma_commit(&ms->pv_done[gx & 1]);
+        mma_commit(&ms->empty[gx & 1]);
+        return true;
+      };
+      int g = 0, k = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(r, c, G);
+        if (u >= U || ms->abort) break;
+        const Unit x = unit_at(p, u);
+        if (!(ok = wait_or_abort(&ms->q_full, k & 1, ms))) break;
+        const int g0 = g;
+        for (int j = 0; j < x.ntiles; ++j, ++g) {
+          const int s = g & 1;
+          if (!(ok = wait_or_abort(&ms->full[s], (g >> 1) & 1, ms))) break;
+          tc_fence_after();
+          const uint32_t k_addr = st_addr + s * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 12; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            const uint64_t a = smem_desc(q_addr + off, 16, 1024, Swizzle::k128B);
+            const uint64_t b = smem_desc(k_addr + off, 16, 1024, Swizzle::k128B);
+            mma_f16(tmem + s * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&ms->s_full[s]);
+          if (j == x.ntiles - 1) mma_commit(&ms->q_free);
+          if (j >= 1 && !(ok = pv(g - 1, j == 1))) break;
+        }
+        if (!ok) break;
+        if (!(ok = pv(g - 1, x.ntiles == 1))) break;
+        (void)g0;
+        ++k;
+      }
+    }
+  } else if (warp >= 4) {
+    // ---- softmax: warpgroup wg takes keys [64 wg, 64 wg + 64) of every tile ----
+    const int wg = (warp - 4) >> 2;
+    const int row = ((warp & 3) << 5) + lane;  // TMEM lane = query row of the tile
+    const uint32_t lane_addr = (uint32_t)((warp & 3) << 5) << 16;
+    const int prefix = p.L - p.T;
+    int g = 0, pv_seen = -1, pair_phase = 0;
+    auto pair_sync = [&]() -> bool {
+      mbar_arrive(&ms->pair_bar);
+      return wait_or_abort(&ms->pair_bar, (pair_phase++) & 1, ms);
+    };
+    auto wait_pv_upto = [&](int target) -> bool {
+      for (int gg = pv_seen + 1; gg <= target; ++gg) {
+        if (!wait_or_abort(&ms->pv_done[gg & 1], (gg >> 1) & 1, ms)) return false;
+        pv_seen = gg;
+      }
+      return true;
+    };
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int u = unit_of(r, c, G);
+      if (u >= U || ms->abort) break;
+      const Unit x = unit_at(p, u);
+      const int t = x.q0 + row;          // new position of this thread's row
+      const int last_key = prefix + t;   // keys 0..last_key are visible
+      float m_run = -INFINITY, l = 0.f;
+      for (int j = 0; j < x.ntiles; ++j, ++g) {
+        const int sb = g & 1;
+        if (!(ok = wait_or_abort(&ms->s_full[sb], (g >> 1) & 1, ms))) break;
+        tc_fence_after();
+        if (!(ok = wait_pv_upto(g - 2))) break;
+        float v[64];
+        const uint32_t scol = tmem + lane_addr + sb * 128 + wg * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float w[16];
+          tmem_ld16(scol + 16 * q, w);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[16 * q + e] = w[e];
+        }
+        tmem_wait_ld();
+        const int k0 = j * kBN + wg * 64;
+        float mloc = -INFINITY;
+        if (k0 + 63 > last_key) {  // the causal edge crosses this half tile
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            v[e] = (k0 + e <= last_key) ? v[e] * p.scale_log2 : -INFINITY;
+            mloc = fmaxf(mloc, v[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            v[e] *= p.scale_log2;
+            mloc = fmaxf(mloc, v[e]);
+          }
+        }
+        ms->red_max[sb][wg][row] = mloc;
+        if (!(ok = pair_sync())) break;
+        const float mt = fmaxf(ms->red_max[sb][0][row], ms->red_max[sb][1][row]);
+        if (mt > m_run + kRescale) {  // first tile of the unit, or a large jump: rescale
+          if (j > 0) {
+            if (!(ok = wait_pv_upto(g - 1))) break;
+            tc_fence_after();
+            const float f = ex2(m_run - mt);
+            const uint32_t ocol = tmem + lane_addr + kColO + wg * 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float w[16];
+              tmem_ld16(ocol + 16 * q, w);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) w[e] *= f;
+              tmem_st16(ocol + 16 * q, w);
+            }
+            l *= f;
+          }
+          m_run = mt;
+        }
+        // probabilities, packed two bf16 per column over this half's first 32 score columns
+        float pk[32];
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float a = ex2(v[2 * e] - m_run), b = ex2(v[2 * e + 1] - m_run);
+          sum += a + b;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+          pk[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+        }
+        l += sum;
+        const uint32_t pcol = tmem + lane_addr + sb * 128 + wg * 64;
+        {
+          float w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pk[e];
+          tmem_st16(pcol, w);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pk[16 + e];
+          tmem_st16(pcol + 16, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&ms->p_full[sb]);
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l, bf16, and the LSE ----
+      if (!(ok = wait_pv_upto(g - 1))) break;
+      tc_fence_after();
+      ms->red_sum[wg][row] = l;
+      if (!(ok = pair_sync())) break;
+      const float lt = ms->red_sum[0][row] + ms->red_sum[1][row];
+      const float inv = 1.f / lt;
+      const uint32_t ocol = tmem + lane_addr + kColO + wg * 64;
+      uint16_t* orow = p.out + ((int64_t)t * p.H + x.h) * 128 + wg * 64;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float w[16];
+        tmem_ld16(ocol + 16 * q, w);
+        tmem_wait_ld();
+        if (t < p.T) {
+          uint32_t pkd[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(w[2 * e] * inv, w[2 * e + 1] * inv);
+            pkd[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + 16 * q);
+          dst[0] = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+          dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+        }
+      }
+      if (wg == 0 && t < p.T && p.lse)
+        p.lse[(int64_t)t * p.H + x.h] = 0.6931471805599453f * (m_run + log2f(lt));
+      tc_fence_before();
+      if (!(ok = pair_sync())) break;  // both warpgroups have read red_sum
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) p.status[c] = ms->status;
+}
+
+// Cached rows -> latent [L][512] bf16 (the e4m3 values; exact) and RoPE rows [L][64] bf16
+// (e4m3 value x kv_scale, one rounding). One thread per 8 codes of a row.
+__global__ void mha_dequant_kernel(const uint8_t* __restrict__ pool, int64_t num_pages,
+                                   int page_size, const int32_t* __restrict__ page_table, int L,
+                                   float kv_scale, __nv_bfloat16* __restrict__ latent,
+                                   __nv_bfloat16* __restrict__ rope, unsigned* status) {
+  const int64_t items = (int64_t)L * (kD / 8);
+  for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int n = (int)(it / (kD / 8));
+    const int c8 = (int)(it % (kD / 8));
+    const int32_t page = page_table[n / page_size];
+    uint2 raw = make_uint2(0u, 0u);
+    if (page < 0 || page >= num_pages) {
+      atomicCAS(status, 0u, (unsigned)MLA_ERR_BOUNDS);
+    } else {
+      raw = *reinterpret_cast<const uint2*>(pool + ((int64_t)page * page_size + n % page_size) * kD +
+                                            c8 * 8);
+    }
+    float f[8];
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)((w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu), __NV_E4M3);
+      const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+    uint32_t o[4];
+    if (c8 < kDV / 8) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(latent + (int64_t)n * kDV + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i] * kv_scale, f[2 * i + 1] * kv_scale);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(rope + (int64_t)n * 64 + (c8 - kDV / 8) * 8) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+}  // namespace
+
+typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                             CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                             CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time dependency on
+// the driver library).
+static EncodeFn tensor_map_encoder() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// One cuBLAS handle per thread and device (created on first use, kept for the process).
+static cublasHandle_t blas_handle(int dev) {
+  thread_local cublasHandle_t handles[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
+  return handles[dev];
+}
+
+cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches) {
+  const int units = ((a.T + kBM - 1) / kBM) * a.H;
+  const int grid = std::min(num_sms, units);
+  // 1. dequantise (its status word follows the attention CTAs' words and is cleared first)
+  unsigned* dq_status = a.status + grid;
+  cudaError_t e = cudaMemsetAsync(dq_status, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  const int64_t items = (int64_t)a.L * (kD / 8);
+  const int grid1 = (int)std::min<int64_t>((items + 255) / 256, (int64_t)num_sms * 8);
+  mha_dequant_kernel<<<grid1, 256, 0, s>>>(a.pool, a.num_pages, a.page_size, a.page_table, a.L,
+                                           a.kv_scale, reinterpret_cast<__nv_bfloat16*>(a.latent),
+                                           reinterpret_cast<__nv_bfloat16*>(a.rope), dq_status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  // 2. up-projection: kvup (column-major [H*256] x L) = W (column-major [H*256] x 512) x latent
+  cublasHandle_t h = blas_handle(a.device);
+  if (!h || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+  const float alpha = a.kv_scale, beta = 0.f;
+  const int m = a.H * 256;
+  if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, m, a.L, kDV, &alpha, a.w_ukv, CUDA_R_16BF, m,
+                   a.latent, CUDA_R_16BF, kDV, &beta, a.kvup, CUDA_R_16BF, m, CUBLAS_COMPUTE_32F,
+                   CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+    return cudaErrorUnknown;
+  ++*launches;
+  // 3. attention
+  const EncodeFn encode = tensor_map_encoder();
+  if (!encode) return cudaErrorInvalidValue;
+  CUtensorMap mq, mkv, mr;
+  cuuint32_t estr[3] = {1, 1, 1};
+  {
+    cuuint64_t dims[3] = {192, (cuuint64_t)a.H, (cuuint64_t)a.T};
+    cuuint64_t strides[2] = {192 * 2, (cuuint64_t)a.H * 192 * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    if (encode(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {256, (cuuint64_t)a.H, (cuuint64_t)a.L};
+    cuuint64_t strides[2] = {256 * 2, (cuuint64_t)a.H * 256 * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    if (encode(&mkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kvup, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {64, (cuuint64_t)a.L};
+    cuuint64_t strides[1] = {64 * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (encode(&mr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.rope, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  MhaParams p;
+  p.L = a.L;
+  p.T = a.T;
+  p.H = a.H;
+  p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.status = a.status;
+  p.hdr = a.hdr;
+  e = cudaFuncSetAttribute(mha_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const bool prof = a.prof_start && a.prof_stop;
+  if (prof) cudaEventRecord(a.prof_start, s);
+  mha_attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, mq, mkv, mr);
+  e = cudaGetLastError();
+  if (prof) cudaEventRecord(a.prof_stop, s);
+  if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+}  // namespace mla

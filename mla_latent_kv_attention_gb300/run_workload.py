@@ -21,13 +21,16 @@ from mla_latent_kv_attention_gb300 import workloads as W
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("workload", choices=sorted(W.WORKLOADS) + ["cache_append", "top_k_renorm"])
+    ap.add_argument("workload", choices=sorted(W.WORKLOADS) + ["cache_append", "top_k_renorm",
+                                                                 "mha_prefill"])
     ap.add_argument("--iters", type=int, default=5)
     ap.add_argument("--heads", type=int, default=12, help="long_history_decode only")
-    ap.add_argument("--T", type=int, default=8192, help="causal_prefill only")
+    ap.add_argument("--T", type=int, default=8192, help="causal_prefill and mha_prefill only")
     args = ap.parse_args(argv)
     if args.workload == "cache_append":
         return _cache_append(args.iters)
+    if args.workload == "mha_prefill":
+        return _mha_prefill(args.T, args.iters)
     if args.workload == "top_k_renorm":
         return _top_k_renorm(args.iters)
     if args.workload == "long_history_decode":
@@ -70,6 +73,23 @@ def _cache_append(iters: int) -> int:
     st = int(status.item())
     print(f"cache_append: {iters} calls, status {mla.STATUS.get(st, st)}")
     return 0 if st == 0 else 1
+
+
+def _mha_prefill(T: int, iters: int) -> int:
+    """The causal prefill chunk (T new positions on a 32,768 prefix, 12 heads) in the MHA form."""
+    m = W.mha_prefill(T=T)
+    kv = mla.KVCache.from_inputs(m.cache, "cuda")
+    q = m.q.cuda()
+    w = m.w_ukv.cuda()
+    L = int(m.cache.seq_lens[0])
+    ws = torch.zeros(mla.library().mla_prefill_mha_workspace_size(L, m.H, 0), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(iters):
+        mla.mla_prefill_mha(kv, q, w, m.cache.sm_scale, L=L, ws=ws)
+    torch.cuda.synchronize()
+    status = mla.mla_read_status(ws)
+    print(f"mha_prefill: {iters} calls, status {mla.STATUS.get(status, status)}")
+    return 0 if status == 0 else 1
 
 
 def _top_k_renorm(iters: int) -> int:

@@ -19,7 +19,26 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def compare(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+# The MHA-form prefill rounds the up-projected keys and values and the probabilities to
+# bf16 before the tensor cores see them (three more roundings than the absorbed path).
+# Emulating exactly those roundings in float64 on the test cases (tests/test_mha_prefill_gpu)
+# gives relative L2 errors of 2.4e-3 to 3.2e-3 (the output's own bf16 rounding alone is
+# 1.7e-3), and it matches the GPU to three digits where the two were compared. Rows that see
+# few keys carry their keys' roundings whole: the LSE (close to those keys' scores) is off by
+# up to 3.9e-3 x max(1, |lse|), and the output (close to one value row, entries up to ~4) by
+# up to 6.0e-3 x the row's largest entry. Each bound is 1.5x (max abs: 1.66x) the largest
+# emulated error; max abs is relative to max(1, the row's largest |entry|).
+MHA_REL_L2 = 5e-3
+MHA_LSE_REL = 6e-3
+MHA_MAX_ABS_ROW = 1e-2
+
+
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, what="", rel_l2=None, lse_rel=None,
+            max_abs_row=None):
+    """max_abs_row: bound |gpu - oracle| by max_abs_row x max(1, the row's largest |entry|)
+    instead of the absolute MAX_ABS."""
+    rel_bound = REL_L2 if rel_l2 is None else rel_l2
+    lse_bound = LSE_REL if lse_rel is None else lse_rel
     og = to_np(out_gpu) if isinstance(out_gpu, torch.Tensor) else np.asarray(out_gpu, np.float64)
     lg = to_np(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else np.asarray(lse_gpu, np.float64)
     og = og.reshape(out_ref.shape)
@@ -30,11 +49,17 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
     assert np.all(np.isfinite(og)), f"{what}: non-finite outputs"
     denom = np.linalg.norm(out_ref)
     rel = np.linalg.norm(og - out_ref) / denom if denom > 0 else np.linalg.norm(og)
-    mx = float(np.max(np.abs(og - out_ref))) if og.size else 0.0
+    if max_abs_row is None:
+        mx = float(np.max(np.abs(og - out_ref))) if og.size else 0.0
+        mx_bound = MAX_ABS
+    else:
+        row_scale = np.maximum(1.0, np.abs(out_ref).max(axis=-1, keepdims=True))
+        mx = float(np.max(np.abs(og - out_ref) / row_scale)) if og.size else 0.0
+        mx_bound = max_abs_row
     fin = ~empty
     lse_err = np.abs(lg[fin] - lse_ref[fin]) / np.maximum(1.0, np.abs(lse_ref[fin]))
     lmax = float(lse_err.max()) if lse_err.size else 0.0
-    assert rel <= REL_L2, f"{what}: rel L2 {rel:.3e} > {REL_L2}"
-    assert mx <= MAX_ABS, f"{what}: max abs {mx:.3e} > {MAX_ABS}"
-    assert lmax <= LSE_REL, f"{what}: lse rel {lmax:.3e} > {LSE_REL}"
+    assert rel <= rel_bound, f"{what}: rel L2 {rel:.3e} > {rel_bound}"
+    assert mx <= mx_bound, f"{what}: max abs {mx:.3e} > {mx_bound}"
+    assert lmax <= lse_bound, f"{what}: lse rel {lmax:.3e} > {lse_bound}"
     return dict(rel_l2=float(rel), max_abs=mx, lse_rel=lmax)

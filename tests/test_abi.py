@@ -139,3 +139,19 @@ def test_verify_f32_rejects_bad_arguments():
     assert call(ctypes.byref(kv), FAKE, 1, 1, 12, 1.0, None, FAKE, FAKE, 1 << 20, None) == 1  # no out
     assert call(ctypes.byref(kv), FAKE, 1, 1, 12, 1.0, FAKE + 4, FAKE, FAKE, 1 << 20, None) == 1
     assert lib.mla_last_launch_count() == 0
+
+
+def test_prefill_mha_rejects_bad_arguments():
+    lib = mla.library()
+    kv = mla.mla_kv_t(FAKE, 4, 64, FAKE, 4, FAKE, 1.0)
+    call = lib.mla_prefill_mha
+    ws = 1 << 30
+    assert call(ctypes.byref(kv), 100, FAKE, 200, 12, FAKE, 1.0, FAKE, FAKE, FAKE, ws, None) == 1  # L < T
+    assert call(ctypes.byref(kv), 300, FAKE, 200, 12, FAKE, 1.0, FAKE, FAKE, FAKE, ws, None) == 1  # L > capacity
+    assert call(ctypes.byref(kv), 200, FAKE, 100, 17, FAKE, 1.0, FAKE, FAKE, FAKE, ws, None) == 2  # H > 16
+    assert call(ctypes.byref(kv), 200, FAKE, 100, 12, None, 1.0, FAKE, FAKE, FAKE, ws, None) == 1  # no weights
+    assert call(ctypes.byref(kv), 200, FAKE + 8, 100, 12, FAKE, 1.0, FAKE, FAKE, FAKE, ws, None) == 1
+    assert call(ctypes.byref(kv), 200, FAKE, 100, 12, FAKE, 1.0, FAKE, FAKE, FAKE + 16, ws, None) == 3
+    assert call(ctypes.byref(kv), 200, FAKE, 0, 12, FAKE, 1.0, FAKE, FAKE, FAKE, ws, None) == 0  # T = 0
+    assert lib.mla_last_launch_count() == 0
+    assert lib.mla_prefill_mha_workspace_size(-1, 12, 0) == 0
