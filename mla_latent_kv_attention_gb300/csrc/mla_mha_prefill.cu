@@ -15,11 +15,14 @@
 //   2. cuBLAS GEMM (a plain library GEMM): kvup [L][H][256] = kv_scale * latent @ W_ukv.
 //   3. mha_attn_kernel: flash attention on tcgen05. One persistent CTA per SM walks units
 //      of (128 new positions, one head), longest first. Per 128-key tile: S = Q K^T
-//      (M = 128 queries, N = 128 keys, K = 192; twelve kind::f16 MMAs) into one of two TMEM
-//      score buffers; two softmax warpgroups (64 keys each) turn S into bf16 probabilities
-//      written back over the scores they came from; O += P V with P read from TMEM
-//      (A operand) and V from shared memory (MN-major). Lazy rescale: O is rescaled only
-//      when a row's maximum grows by more than 2^8.
+//      (M = 128 queries, N = 128 keys, K = 192; twelve kind::f16 MMAs) into the TMEM score
+//      buffer of the tile's parity. Two softmax warpgroups take the tiles of one parity each,
+//      a whole 128-key row a thread, with a running max, sum and O accumulator of their own
+//      (the key axis split in two interleaved halves, merged by their maxima once per unit),
+//      so no tile needs an exchange between them. Probabilities go back as bf16 over the
+//      scores they came from; O_parity += P V with P read from TMEM (A operand) and V from
+//      shared memory (MN-major). Lazy rescale: an O is rescaled only when its row maximum
+//      grows by more than 2^8.
 #include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -45,18 +48,20 @@ constexpr int kBox = 128 * 128;                // one 64-wide bf16 box of 128 ro
 constexpr int kQBytes = 3 * kBox;              // q: dims 0..63, 64..127, 128..191
 constexpr int kKBytes = 3 * kBox;              // keys: two up-projected boxes, then RoPE
 constexpr int kVBytes = 2 * kBox;              // values: dims 0..63, 64..127
-constexpr int kStageBytes = kKBytes + kVBytes;  // 80 KB
-constexpr int kStages = 2;
-constexpr int kThreads = 384;                  // warp 0 TMA, 1 MMA, 4..11 softmax
-constexpr uint32_t kTmemCols = 512;            // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int kStages = 2;                     // key ring and value ring, two buffers each
+constexpr int kThreads = 384;                  // warp 0 TMA (q, keys), 1 MMA, 2 TMA (values), 4..11 softmax
+constexpr uint32_t kTmemCols = 512;            // S0, S1 [0,256); O0, O1 [256,512)
 constexpr uint32_t kColO = 256;
-constexpr int kOffStages = kQBytes;
-constexpr int kOffMisc = kQBytes + kStages * kStageBytes;
+constexpr int kOffK = kQBytes;
+constexpr int kOffV = kOffK + kStages * kKBytes;
+constexpr int kOffMisc = kOffV + kStages * kVBytes;
 constexpr uint64_t kWaitNs = 1000000000ull;    // every wait gives up after 1 s
 constexpr float kRescale = 8.f;                // log2 growth of a row maximum that forces a rescale
 
 struct Misc {
-  uint64_t full[kStages], empty[kStages];
+  // keys are released when their scores MMA completes, values when their values MMA does,
+  // so the next keys load while a tile's softmax runs
+  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t q_full, q_free;
   uint64_t pair_bar;  // bounded barrier of the two softmax warpgroups (256 arrivals)
@@ -136,12 +141,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ms->full[s], 1);
-      mbar_init(&ms->empty[s], 1);
+      mbar_init(&ms->k_full[s], 1);
+      mbar_init(&ms->k_empty[s], 1);
+      mbar_init(&ms->v_full[s], 1);
+      mbar_init(&ms->v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->s_full[i], 1);
-      mbar_init(&ms->p_full[i], 256);
+      mbar_init(&ms->p_full[i], 128);
       mbar_init(&ms->pv_done[i], 1);
     }
     mbar_init(&ms->q_full, 1);
@@ -175,18 +182,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < x.ntiles; ++j, ++g) {
           const int s = g & 1;
-          if (g >= 2 && !(ok = wait_or_abort(&ms->empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
-          uint8_t* st = smem + kOffStages + s * kStageBytes;
-          mbar_arrive_expect_tx(&ms->full[s], kStageBytes);
+          if (g >= 2 && !(ok = wait_or_abort(&ms->k_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
+          uint8_t* kb = smem + kOffK + s * kKBytes;
+          mbar_arrive_expect_tx(&ms->k_full[s], kKBytes);
           const int n0 = j * kBN;
-          tma_load_3d(st, &map_kv, 0, x.h, n0, &ms->full[s]);
-          tma_load_3d(st + kBox, &map_kv, 64, x.h, n0, &ms->full[s]);
-          tma_load_2d(st + 2 * kBox, &map_rope, 0, n0, &ms->full[s]);
-          tma_load_3d(st + kKBytes, &map_kv, 128, x.h, n0, &ms->full[s]);
-          tma_load_3d(st + kKBytes + kBox, &map_kv, 192, x.h, n0, &ms->full[s]);
+          tma_load_3d(kb, &map_kv, 0, x.h, n0, &ms->k_full[s]);
+          tma_load_3d(kb + kBox, &map_kv, 64, x.h, n0, &ms->k_full[s]);
+          tma_load_2d(kb + 2 * kBox, &map_rope, 0, n0, &ms->k_full[s]);
         }
         if (!ok) break;
         ++k;
+      }
+    }
+  } else if (warp == 2) {
+    // ---- TMA producer of the values ----
+    if (lane == 0) {
+      int g = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(r, c, G);
+        if (u >= U || ms->abort) break;
+        const Unit x = unit_at(p, u);
+        for (int j = 0; j < x.ntiles; ++j, ++g) {
+          const int s = g & 1;
+          if (g >= 2 && !(ok = wait_or_abort(&ms->v_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
+          uint8_t* vb = smem + kOffV + s * kVBytes;
+          mbar_arrive_expect_tx(&ms->v_full[s], kVBytes);
+          tma_load_3d(vb, &map_kv, 128, x.h, j * kBN, &ms->v_full[s]);
+          tma_load_3d(vb + kBox, &map_kv, 192, x.h, j * kBN, &ms->v_full[s]);
+        }
       }
     }
   } else if (warp == 1) {
@@ -195,20 +219,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = instr_desc(1, 1, 0, 0, 128, 128);  // bf16, both K-major
       constexpr uint32_t idesc_pv = instr_desc(1, 1, 0, 1, 128, 128);  // P from TMEM, V MN-major
       const uint32_t q_addr = smem_addr(smem);
-      const uint32_t st_addr = smem_addr(smem + kOffStages);
+      const uint32_t k_base = smem_addr(smem + kOffK);
+      const uint32_t v_base = smem_addr(smem + kOffV);
+      // values MMA of tile gx: P from the score buffer of parity gx & 1 into that parity's
+      // O accumulator; `first`: the first tile of this parity in the unit
       auto pv = [&](int gx, bool first) -> bool {
         if (!wait_or_abort(&ms->p_full[gx & 1], (gx >> 1) & 1, ms)) return false;
+        if (!wait_or_abort(&ms->v_full[gx & 1], (gx >> 1) & 1, ms)) return false;
         tc_fence_after();
-        const uint32_t v_addr = st_addr + (gx & 1) * kStageBytes + kKBytes;
+        const uint32_t v_addr = v_base + (gx & 1) * kVBytes;
         const uint32_t pcol = tmem + (gx & 1) * 128;
+        const uint32_t ocol = tmem + kColO + (gx & 1) * 128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t a = pcol + (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
           const uint64_t b = smem_desc(v_addr + ks * 2048, kBox, 1024, Swizzle::k128B);
-          mma_f16_tmem_a(tmem + kColO, a, b, idesc_pv, (first && ks == 0) ? 0u : 1u);
+          mma_f16_tmem_a(ocol, pcol + ks * 8, b, idesc_pv, (first && ks == 0) ? 0u : 1u);
         }
         mma_commit(&ms->pv_done[gx & 1]);
-        mma_commit(&ms->empty[gx & 1]);
+        mma_commit(&ms->v_empty[gx & 1]);
         return true;
       };
       int g = 0, k = 0;
@@ -221,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g0 = g;
         for (int j = 0; j < x.ntiles; ++j, ++g) {
           const int s = g & 1;
-          if (!(ok = wait_or_abort(&ms->full[s], (g >> 1) & 1, ms))) break;
+          if (!(ok = wait_or_abort(&ms->k_full[s], (g >> 1) & 1, ms))) break;
           tc_fence_after();
-          const uint32_t k_addr = st_addr + s * kStageBytes;
+          const uint32_t k_addr = k_base + s * kKBytes;
 #pragma unroll
           for (int kk = 0; kk < 12; ++kk) {
             const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -232,32 +260,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(tmem + s * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&ms->s_full[s]);
+          mma_commit(&ms->k_empty[s]);
           if (j == x.ntiles - 1) mma_commit(&ms->q_free);
-          if (j >= 1 && !(ok = pv(g - 1, j == 1))) break;
+          if (j >= 1 && !(ok = pv(g - 1, j <= 2))) break;
         }
         if (!ok) break;
-        if (!(ok = pv(g - 1, x.ntiles == 1))) break;
+        if (!(ok = pv(g - 1, x.ntiles <= 2))) break;
         (void)g0;
         ++k;
       }
     }
   } else if (warp >= 4) {
-    // ---- softmax: warpgroup wg takes keys [64 wg, 64 wg + 64) of every tile ----
+    // ---- softmax: warpgroup wg takes the tiles of parity wg, a whole 128-key row a thread,
+    // with its own running max, sum and O accumulator; the two merge once per unit ----
     const int wg = (warp - 4) >> 2;
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane = query row of the tile
     const uint32_t lane_addr = (uint32_t)((warp & 3) << 5) << 16;
+    const uint32_t s_col = tmem + lane_addr + wg * 128;       // this warpgroup's score buffer
+    const uint32_t o_col = tmem + lane_addr + kColO + wg * 128;  // and its O accumulator
     const int prefix = p.L - p.T;
-    int g = 0, pv_seen = -1, pair_phase = 0;
+    int g = 0, mine = 0, pair_phase = 0;  // mine: tiles of this parity so far (pv_done phases)
     auto pair_sync = [&]() -> bool {
       mbar_arrive(&ms->pair_bar);
       return wait_or_abort(&ms->pair_bar, (pair_phase++) & 1, ms);
-    };
-    auto wait_pv_upto = [&](int target) -> bool {
-      for (int gg = pv_seen + 1; gg <= target; ++gg) {
-        if (!wait_or_abort(&ms->pv_done[gg & 1], (gg >> 1) & 1, ms)) return false;
-        pv_seen = gg;
-      }
-      return true;
     };
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -267,103 +292,119 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = x.q0 + row;          // new position of this thread's row
       const int last_key = prefix + t;   // keys 0..last_key are visible
       float m_run = -INFINITY, l = 0.f;
+      bool have = false;                 // this warpgroup took a tile of the unit
       for (int j = 0; j < x.ntiles; ++j, ++g) {
-        const int sb = g & 1;
-        if (!(ok = wait_or_abort(&ms->s_full[sb], (g >> 1) & 1, ms))) break;
+        if ((g & 1) != wg) continue;
+        // the k-th tile of this parity is phase k of this parity's barriers
+        if (!(ok = wait_or_abort(&ms->s_full[wg], mine & 1, ms))) break;
+        // this warpgroup's previous values MMA (it wrote O and read P from the buffer about
+        // to be overwritten) finished before these scores were computed; confirm its phase
+        if (mine > 0 && !(ok = wait_or_abort(&ms->pv_done[wg], (mine - 1) & 1, ms))) break;
         tc_fence_after();
-        if (!(ok = wait_pv_upto(g - 2))) break;
-        float v[64];
-        const uint32_t scol = tmem + lane_addr + sb * 128 + wg * 64;
+        const int k0 = j * kBN;
+        const bool edge = k0 + kBN - 1 > last_key;  // the causal edge crosses this tile
+        // pass 1: the row maximum (log2 units)
+        float mt = -INFINITY;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float w[16];
-          tmem_ld16(scol + 16 * q, w);
+          float a[16], b[16];
+          tmem_ld16(s_col + 32 * q, a);
+          tmem_ld16(s_col + 32 * q + 16, b);
+          tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[16 * q + e] = w[e];
-        }
-        tmem_wait_ld();
-        const int k0 = j * kBN + wg * 64;
-        float mloc = -INFINITY;
-        if (k0 + 63 > last_key) {  // the causal edge crosses this half tile
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            v[e] = (k0 + e <= last_key) ? v[e] * p.scale_log2 : -INFINITY;
-            mloc = fmaxf(mloc, v[e]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            v[e] *= p.scale_log2;
-            mloc = fmaxf(mloc, v[e]);
+          for (int e = 0; e < 16; ++e) {
+            const bool va = !edge || k0 + 32 * q + e <= last_key;
+            const bool vb = !edge || k0 + 32 * q + 16 + e <= last_key;
+            mt = fmaxf(mt, va ? a[e] : -INFINITY);
+            mt = fmaxf(mt, vb ? b[e] : -INFINITY);
           }
         }
-        ms->red_max[sb][wg][row] = mloc;
-        if (!(ok = pair_sync())) break;
-        const float mt = fmaxf(ms->red_max[sb][0][row], ms->red_max[sb][1][row]);
-        if (mt > m_run + kRescale) {  // first tile of the unit, or a large jump: rescale
-          if (j > 0) {
-            if (!(ok = wait_pv_upto(g - 1))) break;
-            tc_fence_after();
+        mt *= p.scale_log2;
+        if (mt > m_run + kRescale) {  // first tile, or a large jump: rescale this O
+          if (have) {
             const float f = ex2(m_run - mt);
-            const uint32_t ocol = tmem + lane_addr + kColO + wg * 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
               float w[16];
-              tmem_ld16(ocol + 16 * q, w);
+              tmem_ld16(o_col + 16 * q, w);
               tmem_wait_ld();
 #pragma unroll
               for (int e = 0; e < 16; ++e) w[e] *= f;
-              tmem_st16(ocol + 16 * q, w);
+              tmem_st16(o_col + 16 * q, w);
             }
             l *= f;
           }
           m_run = mt;
         }
-        // probabilities, packed two bf16 per column over this half's first 32 score columns
-        float pk[32];
+        // pass 2: probabilities, packed two bf16 per column over the first 64 score columns
+        // (column 16q + i holds keys 32q + 2i, 32q + 2i + 1; chunk q's packed columns only
+        // overlap score columns already read)
         float sum = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float a = ex2(v[2 * e] - m_run), b = ex2(v[2 * e + 1] - m_run);
-          sum += a + b;
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-          pk[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+        for (int q = 0; q < 4; ++q) {
+          float a[16], b[16];
+          tmem_ld16(s_col + 32 * q, a);
+          tmem_ld16(s_col + 32 * q + 16, b);
+          tmem_wait_ld();
+          float pk[16];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float x0 = a[2 * e] * p.scale_log2 - m_run, x1 = a[2 * e + 1] * p.scale_log2 - m_run;
+            float y0 = b[2 * e] * p.scale_log2 - m_run, y1 = b[2 * e + 1] * p.scale_log2 - m_run;
+            if (edge) {
+              const int kb = k0 + 32 * q + 2 * e;
+              if (kb > last_key) x0 = -INFINITY;
+              if (kb + 1 > last_key) x1 = -INFINITY;
+              if (kb + 16 > last_key) y0 = -INFINITY;
+              if (kb + 17 > last_key) y1 = -INFINITY;
+            }
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(y0), p3 = ex2(y1);
+            sum += (p0 + p1) + (p2 + p3);
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
+            pk[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h0));
+            pk[8 + e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
+          }
+          tmem_st16(s_col + 16 * q, pk);
         }
         l += sum;
-        const uint32_t pcol = tmem + lane_addr + sb * 128 + wg * 64;
-        {
-          float w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pk[e];
-          tmem_st16(pcol, w);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pk[16 + e];
-          tmem_st16(pcol + 16, w);
-        }
+        have = true;
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&ms->p_full[sb]);
+        mbar_arrive(&ms->p_full[wg]);
+        ++mine;
       }
       if (!ok) break;
-      // ---- epilogue: O / l, bf16, and the LSE ----
-      if (!(ok = wait_pv_upto(g - 1))) break;
-      tc_fence_after();
-      ms->red_sum[wg][row] = l;
+      // ---- epilogue: both warpgroups' (m, l, O) merge; warpgroup wg writes dims 64 wg.. ----
+      if (have && !(ok = wait_or_abort(&ms->pv_done[wg], (mine - 1) & 1, ms))) break;
+      tc_fence_before();
+      ms->red_max[0][wg][row] = have ? m_run : -INFINITY;
+      ms->red_sum[wg][row] = have ? l : 0.f;
       if (!(ok = pair_sync())) break;
-      const float lt = ms->red_sum[0][row] + ms->red_sum[1][row];
+      tc_fence_after();
+      const float m0 = ms->red_max[0][0][row], m1 = ms->red_max[0][1][row];
+      const float mm = fmaxf(m0, m1);
+      const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mm);
+      const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mm);
+      const float lt = ms->red_sum[0][row] * f0 + ms->red_sum[1][row] * f1;
       const float inv = 1.f / lt;
-      const uint32_t ocol = tmem + lane_addr + kColO + wg * 64;
+      const float w0 = f0 * inv, w1 = f1 * inv;
       uint16_t* orow = p.out + ((int64_t)t * p.H + x.h) * 128 + wg * 64;
+      const uint32_t oa = tmem + lane_addr + kColO + wg * 64;  // O0, dims of this warpgroup
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        float w[16];
-        tmem_ld16(ocol + 16 * q, w);
+        float a[16], b[16];
+        tmem_ld16(oa + 16 * q, a);
+        tmem_ld16(oa + 128 + 16 * q, b);
         tmem_wait_ld();
         if (t < p.T) {
           uint32_t pkd[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(w[2 * e] * inv, w[2 * e + 1] * inv);
+            // an accumulator that took no tile holds stale values: its weight is exactly 0
+            const float v0 = (w0 != 0.f ? a[2 * e] * w0 : 0.f) + (w1 != 0.f ? b[2 * e] * w1 : 0.f);
+            const float v1 = (w0 != 0.f ? a[2 * e + 1] * w0 : 0.f) + (w1 != 0.f ? b[2 * e + 1] * w1 : 0.f);
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
             pkd[e] = *reinterpret_cast<const uint32_t*>(&h2);
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + 16 * q);
@@ -372,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (wg == 0 && t < p.T && p.lse)
-        p.lse[(int64_t)t * p.H + x.h] = 0.6931471805599453f * (m_run + log2f(lt));
+        p.lse[(int64_t)t * p.H + x.h] = 0.6931471805599453f * (mm + log2f(lt));
       tc_fence_before();
-      if (!(ok = pair_sync())) break;  // both warpgroups have read red_sum
+      if (!(ok = pair_sync())) break;  // both have read the shared (m, l) and both O's
     }
   }
 
