@@ -376,6 +376,42 @@ def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
                              "frac_of_bf16_peak": tf / bf16_peak,
                              "algorithmic_flops": flops, "T": inp.n_q, "prefix": 32768, "H": inp.H}
     del kv, q, out, lse, ws
+    # the same chunk in the MHA form (latent up-projected per head, then causal attention):
+    # the whole call (dequantise + up-projection GEMM + attention) and the attention kernel
+    # alone (library events around its launch)
+    m = W.mha_prefill()
+    kv = mla.KVCache.from_inputs(m.cache, dev)
+    q, w = m.q.to(dev), m.w_ukv.to(dev)
+    L = int(m.cache.seq_lens[0])
+    ws = torch.zeros(mla.library().mla_prefill_mha_workspace_size(L, m.H, dev.index or 0),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(m.T, m.H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(m.T, m.H, dtype=torch.float32, device=dev)
+
+    def mha_call(i):
+        mla.mla_prefill_mha(kv, q, w, m.cache.sm_scale, L=L, out=out, lse=lse, ws=ws)
+
+    ms = _time_events(mha_call, max(3, steps // 5), 2)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record()
+    k1.record()
+    kms = []
+    for _ in range(3):
+        mla.mla_set_profile_events(k0, k1)
+        mha_call(0)
+        mla.mla_set_profile_events(None, None)
+        torch.cuda.synchronize()
+        kms.append(k0.elapsed_time(k1))
+    kms = sorted(kms)[1]
+    aflops = accounting.mha_attention_flops(m.T, L, m.H)
+    pflops = accounting.mha_projection_flops(L, m.H)
+    res["mha_prefill"] = {"ms_per_chunk": ms, "tok_s": m.T / (ms / 1e3),
+                          "attn_kernel_ms": kms, "attn_TFLOP_s": aflops / (kms / 1e3) / 1e12,
+                          "attn_frac_of_bf16_peak": aflops / (kms / 1e3) / 1e12 / bf16_peak,
+                          "whole_call_TFLOP_s": (aflops + pflops) / (ms / 1e3) / 1e12,
+                          "attention_flops": aflops, "projection_flops": pflops,
+                          "T": m.T, "prefix": L - m.T, "H": m.H}
+    del kv, q, w, ws, out, lse
     # appending new rows to the cache: a prefill chunk's 8,192 rows and a decode step's 32,
     # into a pool larger than L2 (each call writes a different set of slots)
     g = torch.Generator().manual_seed(7)

@@ -49,3 +49,22 @@ def attention_flops(seq_lens, n_q: int, H: int) -> int:
 def prefill_bytes(T: int, H: int, L: int) -> int:
     """Queries + cache rows + outputs + LSE of one causal prefill chunk."""
     return T * H * D * 2 + L * D + T * H * DV * 2 + T * H * 4
+
+
+# MHA (non-absorbed) form: per head, keys of 128 up-projected + 64 RoPE dims, values of 128
+# ("MI355X Kimi K2.5 vLLM AITER 7x speedup", section "PR #35850 修复了什么": K and V share
+# one latent, which the MHA form expands per head).
+MHA_QK = 192
+MHA_V = 128
+MHA_FLOPS_PER_PAIR = 2 * (MHA_QK + MHA_V)
+
+
+def mha_attention_flops(T: int, L: int, H: int) -> int:
+    """Score and value flops of the MHA-form causal prefill: T new positions, the last T
+    of L cached, H heads."""
+    return visible_pairs([L], T, H) * MHA_FLOPS_PER_PAIR
+
+
+def mha_projection_flops(L: int, H: int) -> int:
+    """The up-projection of L cached latent rows (512 wide) to H heads x (128 + 128)."""
+    return 2 * L * DV * H * (128 + MHA_V)

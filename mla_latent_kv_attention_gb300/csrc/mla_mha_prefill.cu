@@ -102,23 +102,31 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Mi
   return false;
 }
 
-// Units: (query tile, head), ordered longest first (the last query tile sees the most keys),
-// dealt to the CTAs in a snake: round r gives unit r*G + c to CTA c for even r and to CTA
-// G-1-c for odd r.
+// Units: a pair of adjacent query tiles (2i, 2i+1) of one head, taken by the two CTAs of a
+// cluster (rank 0 the later tile, rank 1 the earlier), which stream the same key and value
+// tiles: each CTA loads half of every tile and multicasts it to both. The pair covers the
+// later tile's keys; for the earlier tile the extra last tile is fully masked. Pairs are
+// ordered longest first and dealt to the clusters in a snake: round r gives pair r*G + c to
+// cluster c for even r and to cluster G-1-c for odd r. With an odd number of query tiles
+// the last pair holds one tile, which rank 1 repeats without writing it.
 struct Unit {
   int q0, h, ntiles;
+  bool write;
 };
 
 __device__ __forceinline__ int num_qtiles(const MhaParams& p) { return (p.T + kBM - 1) / kBM; }
+__device__ __forceinline__ int num_pairs(const MhaParams& p) { return (num_qtiles(p) + 1) / 2; }
 
-__device__ __forceinline__ Unit unit_at(const MhaParams& p, int u) {
+__device__ __forceinline__ Unit unit_at(const MhaParams& p, int u, int rank) {
   const int nq = num_qtiles(p);
+  const int qp = num_pairs(p) - 1 - u / p.H;
+  const int hi = min(2 * qp + 1, nq - 1);         // the pair's later query tile
   Unit x;
-  const int qt = nq - 1 - u / p.H;
   x.h = u % p.H;
-  x.q0 = qt * kBM;
-  const int last = min(x.q0 + kBM, p.T) - 1;      // last new position of the tile
-  const int keys = p.L - p.T + last + 1;           // keys the last position sees
+  x.q0 = (rank == 0 ? hi : 2 * qp) * kBM;
+  x.write = rank == 0 || hi != 2 * qp;
+  const int last = min(hi * kBM + kBM, p.T) - 1;  // last new position of the later tile
+  const int keys = p.L - p.T + last + 1;           // keys it sees
   x.ntiles = (keys + kBN - 1) / kBN;
   return x;
 }
@@ -136,15 +144,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   Misc* ms = reinterpret_cast<Misc*>(smem + kOffMisc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int U = num_qtiles(p) * p.H;
+  const int G = gridDim.x / 2, c = blockIdx.x / 2;  // clusters of two CTAs
+  const int rank = (int)cluster_ctarank();
+  const int U = num_pairs(p) * p.H;
+  constexpr uint16_t kBoth = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ms->k_full[s], 1);
-      mbar_init(&ms->k_empty[s], 1);
+      mbar_init(&ms->k_empty[s], 2);  // both CTAs' MMAs release a buffer both of them fill
       mbar_init(&ms->v_full[s], 1);
-      mbar_init(&ms->v_empty[s], 1);
+      mbar_init(&ms->v_empty[s], 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->s_full[i], 1);
@@ -160,11 +170,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&map_q);
     prefetch_tensormap(&map_kv);
     prefetch_tensormap(&map_rope);
-    if (c == 0) p.hdr->num_ctas = G + 1;  // + the dequantisation's status word
+    if (blockIdx.x == 0) p.hdr->num_ctas = gridDim.x + 1;  // + the dequantisation's status word
   }
   if (warp == 1) tmem_alloc(&ms->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before anything is multicast to them
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
 
@@ -175,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0;; ++r) {
         const int u = unit_of(r, c, G);
         if (u >= U || ms->abort) break;
-        const Unit x = unit_at(p, u);
+        const Unit x = unit_at(p, u, rank);
         if (k > 0 && !wait_or_abort(&ms->q_free, (k - 1) & 1, ms)) break;
         mbar_arrive_expect_tx(&ms->q_full, kQBytes);
         for (int b = 0; b < 3; ++b) tma_load_3d(smem + b * kBox, &map_q, 64 * b, x.h, x.q0, &ms->q_full);
@@ -184,11 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g & 1;
           if (g >= 2 && !(ok = wait_or_abort(&ms->k_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* kb = smem + kOffK + s * kKBytes;
-          mbar_arrive_expect_tx(&ms->k_full[s], kKBytes);
+          mbar_arrive_expect_tx(&ms->k_full[s], kKBytes);  // both halves land here
           const int n0 = j * kBN;
-          tma_load_3d(kb, &map_kv, 0, x.h, n0, &ms->k_full[s]);
-          tma_load_3d(kb + kBox, &map_kv, 64, x.h, n0, &ms->k_full[s]);
-          tma_load_2d(kb + 2 * kBox, &map_rope, 0, n0, &ms->k_full[s]);
+          if (rank == 0) {
+            tma_load_3d_mc(kb, &map_kv, 0, x.h, n0, &ms->k_full[s], kBoth);
+            tma_load_2d_mc(kb + 2 * kBox, &map_rope, 0, n0, &ms->k_full[s], kBoth);
+          } else {
+            tma_load_3d_mc(kb + kBox, &map_kv, 64, x.h, n0, &ms->k_full[s], kBoth);
+          }
         }
         if (!ok) break;
         ++k;
@@ -202,14 +216,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok; ++r) {
         const int u = unit_of(r, c, G);
         if (u >= U || ms->abort) break;
-        const Unit x = unit_at(p, u);
+        const Unit x = unit_at(p, u, rank);
         for (int j = 0; j < x.ntiles; ++j, ++g) {
           const int s = g & 1;
           if (g >= 2 && !(ok = wait_or_abort(&ms->v_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* vb = smem + kOffV + s * kVBytes;
           mbar_arrive_expect_tx(&ms->v_full[s], kVBytes);
-          tma_load_3d(vb, &map_kv, 128, x.h, j * kBN, &ms->v_full[s]);
-          tma_load_3d(vb + kBox, &map_kv, 192, x.h, j * kBN, &ms->v_full[s]);
+          tma_load_3d_mc(vb + rank * kBox, &map_kv, 128 + 64 * rank, x.h, j * kBN, &ms->v_full[s], kBoth);
         }
       }
     }
@@ -235,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = smem_desc(v_addr + ks * 2048, kBox, 1024, Swizzle::k128B);
           mma_f16_tmem_a(ocol, pcol + ks * 8, b, idesc_pv, (first && ks == 0) ? 0u : 1u);
         }
+        mma_commit_mc(&ms->v_empty[gx & 1], kBoth);
         mma_commit(&ms->pv_done[gx & 1]);
-        mma_commit(&ms->v_empty[gx & 1]);
         return true;
       };
       int g = 0, k = 0;
@@ -244,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok; ++r) {
         const int u = unit_of(r, c, G);
         if (u >= U || ms->abort) break;
-        const Unit x = unit_at(p, u);
+        const Unit x = unit_at(p, u, rank);
         if (!(ok = wait_or_abort(&ms->q_full, k & 1, ms))) break;
         const int g0 = g;
         for (int j = 0; j < x.ntiles; ++j, ++g) {
@@ -260,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(tmem + s * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&ms->s_full[s]);
-          mma_commit(&ms->k_empty[s]);
+          mma_commit_mc(&ms->k_empty[s], kBoth);
           if (j == x.ntiles - 1) mma_commit(&ms->q_free);
           if (j >= 1 && !(ok = pv(g - 1, j <= 2))) break;
         }
@@ -288,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; ok; ++r) {
       const int u = unit_of(r, c, G);
       if (u >= U || ms->abort) break;
-      const Unit x = unit_at(p, u);
+      const Unit x = unit_at(p, u, rank);
       const int t = x.q0 + row;          // new position of this thread's row
       const int last_key = prefix + t;   // keys 0..last_key are visible
       float m_run = -INFINITY, l = 0.f;
@@ -397,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(oa + 16 * q, a);
         tmem_ld16(oa + 128 + 16 * q, b);
         tmem_wait_ld();
-        if (t < p.T) {
+        if (x.write && t < p.T) {
           uint32_t pkd[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -412,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
         }
       }
-      if (wg == 0 && t < p.T && p.lse)
+      if (wg == 0 && x.write && t < p.T && p.lse)
         p.lse[(int64_t)t * p.H + x.h] = 0.6931471805599453f * (mm + log2f(lt));
       tc_fence_before();
       if (!(ok = pair_sync())) break;  // both have read the shared (m, l) and both O's
@@ -421,9 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA leaves while the other may still multicast into it or release its buffers;
+  // after an abort, give loads already in flight a moment to land
+  cluster_sync();
+  if (ms->abort && threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000) {
+    }
+  }
+  __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-  if (threadIdx.x == 0) p.status[c] = ms->status;
+  if (threadIdx.x == 0) p.status[blockIdx.x] = ms->status;
 }
 
 // Cached rows -> latent [L][512] bf16 (the e4m3 values; exact) and RoPE rows [L][64] bf16
@@ -508,8 +530,8 @@ static cublasHandle_t blas_handle(int dev) {
 }
 
 cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches) {
-  const int units = ((a.T + kBM - 1) / kBM) * a.H;
-  const int grid = std::min(num_sms, units);
+  const int pairs = (((a.T + kBM - 1) / kBM) + 1) / 2 * a.H;
+  const int grid = 2 * std::min(num_sms / 2, pairs);  // clusters of two CTAs
   // 1. dequantise (its status word follows the attention CTAs' words and is cleared first)
   unsigned* dq_status = a.status + grid;
   cudaError_t e = cudaMemsetAsync(dq_status, 0, sizeof(unsigned), s);
@@ -577,8 +599,19 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
   if (e != cudaSuccess) return e;
   const bool prof = a.prof_start && a.prof_stop;
   if (prof) cudaEventRecord(a.prof_start, s);
-  mha_attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, mq, mkv, mr);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mha_attn_kernel, p, mq, mkv, mr);
   if (prof) cudaEventRecord(a.prof_stop, s);
   if (e == cudaSuccess) ++*launches;
   return e;
