@@ -17,6 +17,7 @@ path. `--impl reference` times the float64 CPU oracle on the same workload inste
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -510,10 +511,23 @@ def cpu_baseline(line):
         if time.perf_counter() - t0 > 10.0 or reps >= 200:
             break
     dt = (time.perf_counter() - t0) / reps
+    # the same oracle on one core, on a bounded sample: the first 4 sequences (about 5 s)
+    small = dataclasses.replace(inp, page_table=inp.page_table[:4], seq_lens=inp.seq_lens[:4],
+                                q=inp.q[:4])
+    nb1 = accounting.decode_bytes(small.seq_lens.tolist(), 1, small.H)
+    r1, t1 = 0, time.perf_counter()
+    while True:
+        oracle.attention(small, n_threads=1)
+        r1 += 1
+        if time.perf_counter() - t1 > 5.0 or r1 >= 50:
+            break
+    dt1 = (time.perf_counter() - t1) / r1
     line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores,
                             "kind": "oracle", "seconds_per_pass": dt, "passes": reps,
                             "sample": "whole workload (32 sequences x 12 heads, float64), "
-                                      f"{reps} passes"}
+                                      f"{reps} passes",
+                            "one_core": {"value": nb1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                                         "sample": f"first 4 sequences x 12 heads, {r1} passes"}}
 
 
 def main():
