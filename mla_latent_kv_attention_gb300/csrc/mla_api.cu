@@ -193,6 +193,8 @@ mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, in
   a.latent = base + w.latent;
   a.rope = base + w.rope;
   a.kvup = base + w.kvup;
+  a.part_out = base + w.part_out;
+  a.part_lse = base + w.part_lse;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.status = reinterpret_cast<unsigned*>(base + w.status);

@@ -123,10 +123,12 @@ __host__ __device__ __forceinline__ int64_t range_of(int64_t x, int64_t total, i
 }
 
 // MHA-form prefill workspace: header, status words (one per attention CTA, then one for the
-// dequantisation), the dequantised latent [L][512] bf16, the RoPE rows [L][64] bf16 and the
-// up-projected keys and values [L][H][256] bf16 (per head 128 key dims, then 128 value dims).
+// dequantisation), the dequantised latent [L][512] bf16, the RoPE rows [L][64] bf16, the
+// up-projected keys and values [L][H][256] bf16 (per head 128 key dims, then 128 value
+// dims), and the partials of units split along the key axis: one slot per cluster of two
+// CTAs, each [2][128][128] float32 outputs and [2][128] float32 LSE.
 struct MhaWsLayout {
-  size_t status, latent, rope, kvup, total;
+  size_t status, latent, rope, kvup, part_out, part_lse, total;
 };
 inline MhaWsLayout mha_ws_layout(int64_t L, int H, int num_sms) {
   MhaWsLayout w;
@@ -139,6 +141,11 @@ inline MhaWsLayout mha_ws_layout(int64_t L, int H, int num_sms) {
   off = align_up(off + (size_t)L * 64 * 2, 256);
   w.kvup = off;
   off = align_up(off + (size_t)L * H * 256 * 2, 256);
+  const size_t slots = (size_t)(num_sms / 2 + 1);
+  w.part_out = off;
+  off = align_up(off + slots * 2 * 128 * 128 * sizeof(float), 256);
+  w.part_lse = off;
+  off = align_up(off + slots * 2 * 128 * sizeof(float), 256);
   w.total = off;
   return w;
 }
@@ -156,6 +163,8 @@ struct MhaArgs {
   void* latent;
   void* rope;
   void* kvup;
+  void* part_out;     // partials of split units (see MhaWsLayout)
+  void* part_lse;
   uint16_t* out;      // [T][H][128] bf16
   float* lse;         // [T][H] or null
   unsigned* status;   // [num attention CTAs + 1]

@@ -89,6 +89,8 @@ struct MhaParams {
   float* lse;        // [T][H] or null
   unsigned* status;  // [gridDim.x]
   WsHeader* hdr;
+  float* part_out;   // [chunks][2][128][128]: normalised partial outputs of split units
+  float* part_lse;   // [chunks][2][128]
 };
 
 __device__ __forceinline__ void report(Misc* m, mla_status_t code) {
@@ -135,6 +137,75 @@ __device__ __forceinline__ int unit_of(int r, int c, int G) {
   return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
+// The work of a cluster: whole units for the full rounds of the snake; the units left over
+// for a last, part-full round are cut along the key axis instead, into as many chunks as
+// fit one per cluster (chunk c of leftover unit c % lo: key tiles [kc n / nch,
+// (kc + 1) n / nch), kc = c / lo), each writing a normalised partial and its LSE to slot
+// c, merged afterwards. This keeps every cluster busy to the end.
+struct Split {
+  int full_rounds, leftover, chunks_per_unit;  // chunks_per_unit < 2: leftovers run whole
+};
+
+__host__ __device__ __forceinline__ int mha_ntiles(int L, int T, int hi_tile) {
+  const int last = (hi_tile * kBM + kBM < T ? hi_tile * kBM + kBM : T) - 1;
+  return (L - T + last + 1 + kBN - 1) / kBN;
+}
+
+__host__ __device__ __forceinline__ Split split_of(int L, int T, int H, int clusters) {
+  const int nq = (T + kBM - 1) / kBM, npairs = (nq + 1) / 2;
+  const int U = npairs * H;
+  Split sp;
+  sp.full_rounds = U / clusters;
+  sp.leftover = U % clusters;
+  sp.chunks_per_unit = 1;
+  if (sp.leftover > 0) {
+    // the last unit (the smallest pair, 2 * 0 and 1) bounds how finely a unit can be cut
+    const int fewest = mha_ntiles(L, T, nq > 1 ? 1 : 0);
+    const int c = clusters / sp.leftover;
+    sp.chunks_per_unit = c < fewest ? c : fewest;
+  }
+  return sp;
+}
+
+struct Work {
+  Unit x;
+  int j0, j1;  // key tiles [j0, j1)
+  int slot;    // -1: the whole unit, written as the final output; else a partial slot
+  bool valid;
+};
+
+__device__ __forceinline__ Work work_at(const MhaParams& p, const Split& sp, int i, int c, int NC,
+                                        int rank) {
+  Work w;
+  w.valid = false;
+  w.slot = -1;
+  if (i < sp.full_rounds) {
+    w.x = unit_at(p, unit_of(i, c, NC), rank);
+    w.j0 = 0;
+    w.j1 = w.x.ntiles;
+    w.valid = true;
+    return w;
+  }
+  if (i > sp.full_rounds || sp.leftover == 0) return w;
+  const int base = sp.full_rounds * NC;
+  if (sp.chunks_per_unit < 2) {
+    if (c >= sp.leftover) return w;
+    w.x = unit_at(p, base + c, rank);
+    w.j0 = 0;
+    w.j1 = w.x.ntiles;
+    w.valid = true;
+    return w;
+  }
+  if (c >= sp.leftover * sp.chunks_per_unit) return w;
+  const int lu = c % sp.leftover, kc = c / sp.leftover;
+  w.x = unit_at(p, base + lu, rank);
+  w.j0 = kc * w.x.ntiles / sp.chunks_per_unit;
+  w.j1 = (kc + 1) * w.x.ntiles / sp.chunks_per_unit;
+  w.slot = c;
+  w.valid = true;
+  return w;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mha_attn_kernel(const MhaParams p, const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kv,
@@ -146,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x / 2, c = blockIdx.x / 2;  // clusters of two CTAs
   const int rank = (int)cluster_ctarank();
-  const int U = num_pairs(p) * p.H;
+  const Split sp = split_of(p.L, p.T, p.H, G);
   constexpr uint16_t kBoth = 0x3;
 
   if (threadIdx.x == 0) {
@@ -184,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int g = 0, k = 0;
       for (int r = 0;; ++r) {
-        const int u = unit_of(r, c, G);
-        if (u >= U || ms->abort) break;
-        const Unit x = unit_at(p, u, rank);
+        const Work wk = work_at(p, sp, r, c, G, rank);
+        if (!wk.valid || ms->abort) break;
+        const Unit& x = wk.x;
         if (k > 0 && !wait_or_abort(&ms->q_free, (k - 1) & 1, ms)) break;
         mbar_arrive_expect_tx(&ms->q_full, kQBytes);
         for (int b = 0; b < 3; ++b) tma_load_3d(smem + b * kBox, &map_q, 64 * b, x.h, x.q0, &ms->q_full);
         bool ok = true;
-        for (int j = 0; j < x.ntiles; ++j, ++g) {
+        for (int j = wk.j0; j < wk.j1; ++j, ++g) {
           const int s = g & 1;
           if (g >= 2 && !(ok = wait_or_abort(&ms->k_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* kb = smem + kOffK + s * kKBytes;
@@ -214,10 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int u = unit_of(r, c, G);
-        if (u >= U || ms->abort) break;
-        const Unit x = unit_at(p, u, rank);
-        for (int j = 0; j < x.ntiles; ++j, ++g) {
+        const Work wk = work_at(p, sp, r, c, G, rank);
+        if (!wk.valid || ms->abort) break;
+        const Unit& x = wk.x;
+        for (int j = wk.j0; j < wk.j1; ++j, ++g) {
           const int s = g & 1;
           if (g >= 2 && !(ok = wait_or_abort(&ms->v_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* vb = smem + kOffV + s * kVBytes;
@@ -255,12 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, k = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int u = unit_of(r, c, G);
-        if (u >= U || ms->abort) break;
-        const Unit x = unit_at(p, u, rank);
+        const Work wk = work_at(p, sp, r, c, G, rank);
+        if (!wk.valid || ms->abort) break;
+        const int n = wk.j1 - wk.j0;  // tiles of this work item
         if (!(ok = wait_or_abort(&ms->q_full, k & 1, ms))) break;
-        const int g0 = g;
-        for (int j = 0; j < x.ntiles; ++j, ++g) {
+        for (int j = 0; j < n; ++j, ++g) {
           const int s = g & 1;
           if (!(ok = wait_or_abort(&ms->k_full[s], (g >> 1) & 1, ms))) break;
           tc_fence_after();
@@ -274,12 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&ms->s_full[s]);
           mma_commit_mc(&ms->k_empty[s], kBoth);
-          if (j == x.ntiles - 1) mma_commit(&ms->q_free);
+          if (j == n - 1) mma_commit(&ms->q_free);
           if (j >= 1 && !(ok = pv(g - 1, j <= 2))) break;
         }
         if (!ok) break;
-        if (!(ok = pv(g - 1, x.ntiles <= 2))) break;
-        (void)g0;
+        if (!(ok = pv(g - 1, n <= 2))) break;
         ++k;
       }
     }
@@ -299,14 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int u = unit_of(r, c, G);
-      if (u >= U || ms->abort) break;
-      const Unit x = unit_at(p, u, rank);
+      const Work wk = work_at(p, sp, r, c, G, rank);
+      if (!wk.valid || ms->abort) break;
+      const Unit& x = wk.x;
       const int t = x.q0 + row;          // new position of this thread's row
       const int last_key = prefix + t;   // keys 0..last_key are visible
       float m_run = -INFINITY, l = 0.f;
-      bool have = false;                 // this warpgroup took a tile of the unit
-      for (int j = 0; j < x.ntiles; ++j, ++g) {
+      bool have = false;                 // this warpgroup took a tile of the work item
+      for (int j = wk.j0; j < wk.j1; ++j, ++g) {
         if ((g & 1) != wg) continue;
         // the k-th tile of this parity is phase k of this parity's barriers
         if (!(ok = wait_or_abort(&ms->s_full[wg], mine & 1, ms))) break;
@@ -400,17 +469,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mm);
       const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mm);
       const float lt = ms->red_sum[0][row] * f0 + ms->red_sum[1][row] * f1;
-      const float inv = 1.f / lt;
+      // a key chunk can hold no visible key for a row: partial 0 with lse -inf (weight 0)
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float w0 = f0 * inv, w1 = f1 * inv;
       uint16_t* orow = p.out + ((int64_t)t * p.H + x.h) * 128 + wg * 64;
       const uint32_t oa = tmem + lane_addr + kColO + wg * 64;  // O0, dims of this warpgroup
+      float* prow = wk.slot >= 0
+                        ? p.part_out + (((int64_t)wk.slot * 2 + rank) * kBM + row) * 128 + wg * 64
+                        : nullptr;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float a[16], b[16];
         tmem_ld16(oa + 16 * q, a);
         tmem_ld16(oa + 128 + 16 * q, b);
         tmem_wait_ld();
-        if (x.write && t < p.T) {
+        if (prow) {  // a partial of a split unit, float32, normalised by its own sum
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            float4 v4;
+            v4.x = (w0 != 0.f ? a[e] * w0 : 0.f) + (w1 != 0.f ? b[e] * w1 : 0.f);
+            v4.y = (w0 != 0.f ? a[e + 1] * w0 : 0.f) + (w1 != 0.f ? b[e + 1] * w1 : 0.f);
+            v4.z = (w0 != 0.f ? a[e + 2] * w0 : 0.f) + (w1 != 0.f ? b[e + 2] * w1 : 0.f);
+            v4.w = (w0 != 0.f ? a[e + 3] * w0 : 0.f) + (w1 != 0.f ? b[e + 3] * w1 : 0.f);
+            *reinterpret_cast<float4*>(prow + 16 * q + e) = v4;
+          }
+        } else if (x.write && t < p.T) {
           uint32_t pkd[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -425,7 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
         }
       }
-      if (wg == 0 && x.write && t < p.T && p.lse)
+      if (wg == 0 && wk.slot >= 0)
+        p.part_lse[((int64_t)wk.slot * 2 + rank) * kBM + row] =
+            lt > 0.f ? 0.6931471805599453f * (mm + log2f(lt)) : -INFINITY;
+      else if (wg == 0 && x.write && t < p.T && p.lse)
         p.lse[(int64_t)t * p.H + x.h] = 0.6931471805599453f * (mm + log2f(lt));
       tc_fence_before();
       if (!(ok = pair_sync())) break;  // both have read the shared (m, l) and both O's
@@ -446,6 +532,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0) p.status[blockIdx.x] = ms->status;
+}
+
+// The split units' partials, merged by their LSE: one warp per query row of a split unit
+// (4 of the 128 dims a lane); lse = m + ln sum_c exp(lse_c - m), out = sum_c exp(lse_c -
+// lse) out_c.
+__global__ void __launch_bounds__(256) mha_chunk_merge_kernel(const MhaParams p, Split sp, int NC) {
+  const int wid = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= sp.leftover * 2 * kBM) return;
+  const int lu = wid / (2 * kBM), rank = (wid / kBM) & 1, row = wid % kBM;
+  const Unit x = unit_at(p, sp.full_rounds * NC + lu, rank);
+  const int t = x.q0 + row;
+  if (!x.write || t >= p.T) return;
+  const int nch = sp.chunks_per_unit;
+  float m = -INFINITY;
+  for (int kc = 0; kc < nch; ++kc)
+    m = fmaxf(m, p.part_lse[((int64_t)(kc * sp.leftover + lu) * 2 + rank) * kBM + row]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float sum = 0.f;
+  for (int kc = 0; kc < nch; ++kc) {
+    const int64_t sr = ((int64_t)(kc * sp.leftover + lu) * 2 + rank) * kBM + row;
+    const float ls = p.part_lse[sr];
+    if (ls == -INFINITY) continue;
+    const float w = expf(ls - m);
+    const float4 v = *reinterpret_cast<const float4*>(p.part_out + sr * 128 + 4 * lane);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+    sum += w;
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.H + x.h) * 128 + 4 * lane) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+  if (lane == 0 && p.lse) p.lse[(int64_t)t * p.H + x.h] = sum > 0.f ? m + logf(sum) : -INFINITY;
 }
 
 // Cached rows -> latent [L][512] bf16 (the e4m3 values; exact) and RoPE rows [L][64] bf16
@@ -595,6 +718,8 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
   p.lse = a.lse;
   p.status = a.status;
   p.hdr = a.hdr;
+  p.part_out = static_cast<float*>(a.part_out);
+  p.part_lse = static_cast<float*>(a.part_lse);
   e = cudaFuncSetAttribute(mha_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const bool prof = a.prof_start && a.prof_stop;
@@ -612,8 +737,16 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, mha_attn_kernel, p, mq, mkv, mr);
-  if (prof) cudaEventRecord(a.prof_stop, s);
   if (e == cudaSuccess) ++*launches;
+  if (prof) cudaEventRecord(a.prof_stop, s);
+  // the split units' partials (only when the last round was cut into chunks)
+  const Split sp = split_of(a.L, a.T, a.H, grid / 2);
+  if (e == cudaSuccess && sp.leftover > 0 && sp.chunks_per_unit >= 2) {
+    const int warps = sp.leftover * 2 * kBM;
+    mha_chunk_merge_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, sp, grid / 2);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) ++*launches;
+  }
   return e;
 }
 

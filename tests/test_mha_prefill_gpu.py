@@ -22,8 +22,10 @@ def run(m):
     return out, lse
 
 
+# (1280, 1000, 16): 80 pairs of query tiles for 76 clusters, so the four pairs of the last
+# round are cut along the key axis and merged from partials
 @pytest.mark.parametrize("T,prefix,H", [(128, 0, 1), (200, 300, 2), (384, 1000, 12), (64, 4096, 16),
-                                        (1, 77, 8), (300, 0, 3), (129, 127, 12)])
+                                        (1, 77, 8), (300, 0, 3), (129, 127, 12), (1280, 1000, 16)])
 def test_mha_prefill_small(T, prefix, H):
     m = W.mha_prefill_inputs(T, prefix, H=H, seed=T + prefix + H)
     out, lse = run(m)
