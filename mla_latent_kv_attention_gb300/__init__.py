@@ -22,6 +22,8 @@ LIB_PATH = os.path.join(_PKG, "libmla.so")
 MLA_D = 576
 MLA_DV = 512
 MLA_OP_DECODE, MLA_OP_VERIFY, MLA_OP_PREFILL = 0, 1, 2
+(MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA,
+ MLA_ERR_TIMEOUT, MLA_ERR_BOUNDS) = range(7)
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT", 6: "MLA_ERR_BOUNDS"}
 

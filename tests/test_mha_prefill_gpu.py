@@ -89,3 +89,32 @@ def test_mha_prefill_reports_no_error():
     mla.mla_prefill_mha(kv, m.q.to(DEV), m.w_ukv.to(DEV), m.cache.sm_scale, ws=ws)
     torch.cuda.synchronize()
     assert mla.mla_read_status(ws) == 0
+
+
+@pytest.mark.parametrize("page_size", [128, 256])
+def test_mha_prefill_larger_pages(page_size):
+    m = W.mha_prefill_inputs(300, 700, H=4, seed=page_size, page_size=page_size)
+    out, lse = run(m)
+    ref_out, ref_lse = oracle.mha_prefill_rows(m.cache, m.q, m.w_ukv)
+    compare(out, lse, ref_out, ref_lse, f"mha pages of {page_size}", rel_l2=MHA_REL_L2,
+            lse_rel=MHA_LSE_REL, max_abs_row=MHA_MAX_ABS_ROW)
+
+
+def test_mha_prefill_reports_a_page_outside_the_pool():
+    """A page-table entry past the pool is reported through the status words; the
+    dequantisation checks the index before it reads, so nothing outside the pool is touched."""
+    m = W.mha_prefill_inputs(64, 200, H=2, seed=5)
+    pt = m.cache.page_table.clone()
+    pt[0, 1] = m.cache.pool.shape[0] + 3
+    kv = mla.KVCache(m.cache.pool.to(DEV), pt.to(DEV), m.cache.seq_lens.to(DEV), m.cache.kv_scale)
+    L = int(m.cache.seq_lens[0])
+    ws = torch.zeros(mla.library().mla_prefill_mha_workspace_size(L, 2, 0), dtype=torch.uint8,
+                     device=DEV)
+    mla.mla_prefill_mha(kv, m.q.to(DEV), m.w_ukv.to(DEV), m.cache.sm_scale, ws=ws)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status(ws) == mla.MLA_ERR_BOUNDS
+    # the next correct call on the same workspace reports no error
+    kv_ok = mla.KVCache.from_inputs(m.cache, DEV)
+    mla.mla_prefill_mha(kv_ok, m.q.to(DEV), m.w_ukv.to(DEV), m.cache.sm_scale, ws=ws)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status(ws) == 0
