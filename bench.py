@@ -291,6 +291,10 @@ def bench_ours(args, world, rank, local):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_per_step_percentiles": {
+                "p10": float(statistics.quantiles(step_ms, n=10)[0]) if len(step_ms) > 1 else step_ms[0],
+                "p50": float(statistics.median(step_ms)),
+                "p90": float(statistics.quantiles(step_ms, n=10)[-1]) if len(step_ms) > 1 else step_ms[0]},
             "us_per_layer": ms * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp32-acc (e4m3 cache, bf16 q/out)",
             "data": "synthetic",
