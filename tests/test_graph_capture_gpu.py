@@ -1,0 +1,66 @@
+"""Every call is stream-ordered and allocation-free on its own path, so it can be captured
+in a CUDA graph: a replay must give bit-identical results to the eager calls."""
+import pytest
+import torch
+
+import mla_latent_kv_attention_gb300 as mla
+from mla_latent_kv_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def test_graph_replay_matches_eager():
+    dec = W.make_inputs("g_dec", [700, 3000, 129], H=12, n_q=1, seed=31)
+    ver = W.make_inputs("g_ver", [900, 4], H=8, n_q=4, seed=32)
+    mha = W.mha_prefill_inputs(300, 500, H=4, seed=33)
+    kd, kv_, km = (mla.KVCache.from_inputs(x, DEV) for x in (dec, ver, mha.cache))
+    qd = dec.q[:, 0].contiguous().to(DEV)
+    qv = ver.q.to(DEV)
+    qm, wm = mha.q.to(DEV), mha.w_ukv.to(DEV)
+    L = int(mha.cache.seq_lens[0])
+    ws_d = mla.workspace(mla.MLA_OP_DECODE, dec.B, dec.H, 1, DEV)
+    ws_v = mla.workspace(mla.MLA_OP_VERIFY, ver.B, ver.H, ver.n_q, DEV)
+    ws_m = torch.zeros(mla.library().mla_prefill_mha_workspace_size(L, mha.H, 0), dtype=torch.uint8,
+                       device=DEV)
+    od = torch.empty(dec.B, dec.H, 512, dtype=torch.bfloat16, device=DEV)
+    ld = torch.empty(dec.B, dec.H, dtype=torch.float32, device=DEV)
+    ov = torch.empty(ver.B, ver.n_q, ver.H, 512, dtype=torch.bfloat16, device=DEV)
+    lv = torch.empty(ver.B, ver.n_q, ver.H, dtype=torch.float32, device=DEV)
+    om = torch.empty(mha.T, mha.H, 128, dtype=torch.bfloat16, device=DEV)
+    lm = torch.empty(mha.T, mha.H, dtype=torch.float32, device=DEV)
+    g = torch.Generator().manual_seed(34)
+    pool = torch.zeros(64, 64, 576, dtype=torch.uint8, device=DEV)
+    rows = torch.randn(40, 576, generator=g).to(torch.bfloat16).to(DEV)
+    slots = torch.randperm(64 * 64, generator=g)[:40].to(DEV)
+    probs = torch.softmax(torch.randn(6, 5000, generator=g), 1).to(DEV)
+    tk = torch.empty_like(probs)
+
+    def calls():
+        mla.mla_decode(kd, qd, dec.sm_scale, out=od, lse=ld, ws=ws_d)
+        mla.mla_verify(kv_, qv, ver.sm_scale, out=ov, lse=lv, ws=ws_v)
+        mla.mla_prefill_mha(km, qm, wm, mha.cache.sm_scale, L=L, out=om, lse=lm, ws=ws_m)
+        mla.mla_cache_append(pool, rows, slots, 0.0125)
+        mla.mla_top_k_renorm_prob(probs, 17, out=tk)
+
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        calls()  # warm: the cuBLAS handle and module loading happen outside the capture
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (od, ld, ov, lv, om, lm, pool, tk)]
+    for t in (od, ld, ov, lv, om, lm, tk):
+        t.zero_()
+    pool.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls()
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, (od, ld, ov, lv, om, lm, pool, tk)):
+        if a.dtype == torch.bfloat16:
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        else:
+            assert torch.equal(a, b)
+    assert mla.mla_read_status(ws_d) == 0 and mla.mla_read_status(ws_v) == 0
+    assert mla.mla_read_status(ws_m) == 0
