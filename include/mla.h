@@ -231,6 +231,15 @@ mla_status_t mla_top_k_renorm_prob(const float* probs, float* out, int B, int V,
  */
 mla_status_t mla_read_status(const void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Test hook for the failure path: the next mla_decode / mla_verify / mla_verify_f32 call on
+ * this thread launches its attention kernel with the key loads switched off, so every wait
+ * on them gives up after its limit (about a second) and the call's status words report
+ * MLA_ERR_TIMEOUT; the kernel still returns, the context stays usable, and the outputs of
+ * that call are undefined. Not for production use.
+ */
+void mla_test_stall_next_call(void);
+
 /* Static, human-readable name of a status code. */
 const char* mla_status_string(mla_status_t status);
 

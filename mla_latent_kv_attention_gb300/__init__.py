@@ -32,7 +32,7 @@ EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla
            "mla_read_status", "mla_status_string", "mla_last_launch_count",
            "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append",
            "mla_top_k_renorm_prob", "mla_verify_f32", "mla_prefill_mha",
-           "mla_prefill_mha_workspace_size")
+           "mla_prefill_mha_workspace_size", "mla_test_stall_next_call")
 
 
 class MlaError(RuntimeError):
@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_prefill_mha_workspace_size.restype = sz
     lib.mla_prefill_mha.argtypes = [KV, i32, P, i32, i32, P, f32, P, P, P, sz, P]
     lib.mla_prefill_mha.restype = i32
+    lib.mla_test_stall_next_call.argtypes = []
+    lib.mla_test_stall_next_call.restype = None
     lib.mla_prefill.argtypes = [KV, P, i32, i32, f32, P, P, P, sz, P]
     lib.mla_merge_lse.argtypes = [P, P, i32, i64, P, P, P]
     lib.mla_read_status.argtypes = [P, sz, P]

@@ -66,6 +66,10 @@ mla_status_t current_device(int* dev) {
   return MLA_OK;
 }
 
+// Set by mla_test_stall_next_call; consumed (and cleared) by the next decode/verify call on
+// this thread.
+thread_local int g_test_stall = 0;
+
 mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H, float sm_scale,
                        void* out, float* lse, void* ws, size_t ws_bytes, void* stream,
                        bool out_is_f32 = false) {
@@ -85,6 +89,8 @@ mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
   if (ws_bytes < w.total) return MLA_ERR_WORKSPACE;
   if (B == 0) return MLA_OK;
   mla::AttnParams p = base_params(kv, q, B, n_q, H, sm_scale, out, lse);
+  p.test_stall = g_test_stall;
+  g_test_stall = 0;
   if (out_is_f32) {
     p.out = nullptr;
     p.out_f32 = static_cast<float*>(out);
@@ -314,6 +320,8 @@ mla_status_t mla_top_k_renorm_prob(const float* probs, float* out, int B, int V,
   ++g_last_launches;
   return MLA_OK;
 }
+
+void mla_test_stall_next_call(void) { g_test_stall = 1; }
 
 mla_status_t mla_read_status(const void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < sizeof(mla::WsHeader)) return MLA_ERR_WORKSPACE;

@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           pf_k += kTileKeys;
         }
       };
-      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && !aborted(ms);
+      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && !aborted(ms) && !p.test_stall;
            cu = next_unit(args, cu)) {
         const UnitInfo un = unit_info(args, ms, cu);
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {

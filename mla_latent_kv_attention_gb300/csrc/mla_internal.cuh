@@ -111,6 +111,8 @@ struct AttnParams {
   int64_t qimg_stride;
   WsHeader* hdr;
   int num_ctas;
+  int test_stall;     // test hook: the producer issues no loads, so every consumer's bounded
+                      // wait runs out and the call reports MLA_ERR_TIMEOUT
 };
 
 // The CTA of a split plan that holds block x, when `total` blocks are cut into n ranges

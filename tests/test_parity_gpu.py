@@ -295,3 +295,22 @@ def test_cuda_graph_replay_matches_eager():
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing satisfies (the test hook switches the key loads off for one call)
+    gives up after its limit: the kernel returns, the status words say MLA_ERR_TIMEOUT, and
+    the next call on the same workspace is correct and clean."""
+    inp = W.make_inputs("stall", [300, 1000], H=12, n_q=1, seed=41)
+    kv = mla.KVCache.from_inputs(inp, DEV)
+    q = inp.q[:, 0].contiguous().to(DEV)
+    ws = mla.workspace(mla.MLA_OP_DECODE, inp.B, inp.H, 1, DEV)
+    mla.library().mla_test_stall_next_call()
+    mla.mla_decode(kv, q, inp.sm_scale, ws=ws)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status(ws) == mla.MLA_ERR_TIMEOUT
+    out, lse = mla.mla_decode(kv, q, inp.sm_scale, ws=ws)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status(ws) == 0
+    ref_out, ref_lse = oracle.attention(inp)
+    compare(out[:, None], lse[:, None], ref_out, ref_lse, "after a timed-out call")
