@@ -24,6 +24,7 @@ CASES = [
     ([2000, 4, 257], 12, 4),
     ([513, 77], 8, 2),
     ([20000] * 3, 12, 1),  # long enough to be split over several CTAs
+    ([3000, 700], 16, 4),  # 64 rows a sequence: two launches over halves of the heads
 ]
 
 
