@@ -168,7 +168,8 @@ mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float 
  *   workspace  device, 256-B aligned, mla_prefill_mha_workspace_size(L, H, device) bytes:
  *          the dequantised latent, the up-projected keys and values, status words.
  * Errors as mla_prefill; a page index outside the pool is reported by mla_read_status.
- * Launches: a dequantisation kernel, one cuBLAS GEMM, the attention kernel.
+ * Launches: a dequantisation kernel, the up-projection GEMM (tcgen05), the attention kernel
+ * (and a merge of key-split units when the last round of units is cut along the keys).
  */
 size_t mla_prefill_mha_workspace_size(int L, int H, int device);
 mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, int H,
@@ -196,8 +197,9 @@ mla_status_t mla_merge_lse(const float* part_out, const float* part_lse, int S, 
  * slots[i] >= 0, cache row slots[i] (page slots[i] / page_size, position slots[i] %
  * page_size) becomes the e4m3 codes of x_i * (1 / kv_scale): the reciprocal and each
  * product are rounded to binary32, the conversion rounds to nearest even and saturates
- * finite values and infinities at +-448 (NaN stays NaN). Rows with a negative slot are
- * skipped (padding).
+ * finite values and infinities at +-448 (NaN stays NaN); this is also how the library's
+ * input generator quantises the rows it draws. Rows with a negative slot are skipped
+ * (padding).
  *   pool    device, [num_pages][page_size][576] e4m3 codes, 16-byte aligned (written)
  *   x       device, [n][576] bfloat16, 16-byte aligned
  *   slots   device, [n] int64 flat cache rows, 8-byte aligned
@@ -256,6 +258,18 @@ int mla_last_launch_count(void);
 void mla_set_profile_events(void* start, void* stop);
 
 /*
+ * Profiling hook. With a device buffer of `bytes` (8-byte aligned), the next decode /
+ * verify / prefill calls on this host thread make each CTA c of their attention kernel
+ * (while c < bytes / 64) write eight 64-bit words at buffer + 64 c: the GPU's global timer
+ * (ns) at entry, after the wait on the previous kernel, after the split plan, when the
+ * first tile's scores were read, when the last tile's probabilities were written, after
+ * its last epilogue and at exit, then (tiles << 32 | units) it processed. NULL switches it
+ * off. The buffer stays owned by the caller; the results are undefined while two calls
+ * overlap on the GPU.
+ */
+void mla_set_trace_buffer(void* device_buffer, size_t bytes);
+
+/*
  * Decode without a caller-provided workspace. (The pages describe no such entry point; it
  * exists for callers of this library that cannot allocate device memory: an engine that
  * has already reserved nearly all device memory for its own pools, or a latency-critical
@@ -268,18 +282,29 @@ void mla_set_profile_events(void* start, void* stop);
  *  - A batch whose mla_workspace_size(MLA_OP_DECODE, B, H, 1, device) exceeds
  *    MLA_STATIC_WS_BYTES is rejected with MLA_ERR_WORKSPACE before anything is enqueued
  *    (16 MiB covers 16-head decode of any batch up to several hundred thousand
- *    sequences on a 152-SM GB300: the partial outputs take about 10 MB of it).
- *  - The first call on each device looks up the array's device address (a runtime
+ *    sequences on a 152-SM GB300: the partial outputs and staged query rows take about
+ *    13 MB of it).
+ *  - The first call on each device (and the first after the device's context changed,
+ *    for instance after cudaDeviceReset) looks up the array's device address (a runtime
  *    symbol query); make that first call outside any CUDA stream capture.
  *  - All calls on a device share the one array, which keeps the previous call's
  *    contents (each call rewrites everything it reads). Calls whose work overlaps on
  *    the GPU (different streams without ordering,
  *    or several host threads) race on it and give wrong results: serialise them.
- *  - The device-side status word of these calls cannot be read with mla_read_status.
+ *  - The device-side status words of these calls (MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT) are
+ *    read with mla_read_status_static.
  */
 #define MLA_STATIC_WS_BYTES (16u << 20)
 mla_status_t mla_decode_static_ws(const mla_kv_t* kv, const void* q, int B, int H,
                                   float sm_scale, void* out, float* lse, void* stream);
+
+/*
+ * mla_read_status for the library-owned workspace of mla_decode_static_ws on the current
+ * device: synchronises `stream`, then returns the status the last mla_decode_static_ws
+ * call on this device left (MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT), or MLA_ERR_CUDA.
+ * Allocates nothing. (No counterpart on the pages, like mla_decode_static_ws.)
+ */
+mla_status_t mla_read_status_static(void* stream);
 
 #ifdef __cplusplus
 }

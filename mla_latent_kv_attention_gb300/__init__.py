@@ -32,7 +32,8 @@ EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla
            "mla_read_status", "mla_status_string", "mla_last_launch_count",
            "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append",
            "mla_top_k_renorm_prob", "mla_verify_f32", "mla_prefill_mha",
-           "mla_prefill_mha_workspace_size", "mla_test_stall_next_call")
+           "mla_prefill_mha_workspace_size", "mla_test_stall_next_call",
+           "mla_read_status_static", "mla_set_trace_buffer")
 
 
 class MlaError(RuntimeError):
@@ -79,6 +80,10 @@ def _load() -> ctypes.CDLL:
     lib.mla_set_profile_events.restype = None
     lib.mla_decode_static_ws.argtypes = [KV, P, i32, i32, f32, P, P, P]
     lib.mla_decode_static_ws.restype = i32
+    lib.mla_read_status_static.argtypes = [P]
+    lib.mla_read_status_static.restype = i32
+    lib.mla_set_trace_buffer.argtypes = [P, sz]
+    lib.mla_set_trace_buffer.restype = None
     lib.mla_cache_append.argtypes = [P, i64, i32, P, P, i64, f32, P, P]
     lib.mla_cache_append.restype = i32
     lib.mla_top_k_renorm_prob.argtypes = [P, P, i32, i32, P, i32, P]

@@ -58,8 +58,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
     if force or jobs or _stale(LIB, objs):
-        # cuBLAS for the MHA-form prefill's up-projection (a plain GEMM)
-        run([nvcc()] + ARCH + ["-shared", "-o", LIB] + objs + ["-lcublas"])
+        run([nvcc()] + ARCH + ["-shared", "-o", LIB] + objs)
     return LIB
 
 

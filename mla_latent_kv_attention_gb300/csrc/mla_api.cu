@@ -9,6 +9,8 @@ namespace {
 
 thread_local int g_last_launches = 0;
 thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+thread_local unsigned long long* g_trace = nullptr;  // mla_set_trace_buffer
+thread_local int g_trace_ctas = 0;
 
 void prof_mark(cudaEvent_t e, cudaStream_t s) {
   if (g_prof_start && g_prof_stop) cudaEventRecord(e, s);
@@ -55,6 +57,8 @@ mla::AttnParams base_params(const mla_kv_t* kv, const void* q, int B, int n_q, i
   p.R = n_q * H;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
+  p.trace = g_trace;
+  p.trace_ctas = g_trace_ctas;
   return p;
 }
 
@@ -367,6 +371,12 @@ int mla_last_launch_count(void) { return g_last_launches; }
 void mla_set_profile_events(void* start, void* stop) {
   g_prof_start = static_cast<cudaEvent_t>(start);
   g_prof_stop = static_cast<cudaEvent_t>(stop);
+}
+
+void mla_set_trace_buffer(void* device_buffer, size_t bytes) {
+  const size_t per_cta = sizeof(unsigned long long) * mla::kTraceWords;
+  g_trace = (device_buffer && bytes >= per_cta) ? static_cast<unsigned long long*>(device_buffer) : nullptr;
+  g_trace_ctas = g_trace ? (int)(bytes / per_cta < 65536 ? bytes / per_cta : 65536) : 0;
 }
 
 }  // extern "C"

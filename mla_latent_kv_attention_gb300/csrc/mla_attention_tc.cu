@@ -9,12 +9,25 @@
 // Both contractions run on the FP8 cache bytes as they are, with no dequantisation pass:
 //   scores  S^T[key][n] = sum_d code[key][d] * Qt[n][d]      tcgen05 kind::f8f6f4,
 //           M = 128 keys, N = 2 x (padded rows), K = 576
-//           The bf16 query row, scaled by a power of two, is split exactly into two e4m3
-//           terms (bf16 has 8 significant bits, e4m3 4), stacked along N and summed after.
+//           The bf16 query row, scaled by the power of two that puts its largest
+//           magnitude in (224, 448], is split into two e4m3 terms stacked along N: the
+//           first is the entry rounded to e4m3, the second the residual times 16 rounded
+//           to e4m3 (the residual is at most 16, so this never saturates), and the two
+//           accumulators are summed as S1 + S2 / 16. The split is exact for every entry of
+//           at least 2^-14.8 of the row's largest magnitude (bf16 has 8 significant bits,
+//           e4m3 4, and the scaled residual is a multiple of e4m3's subnormal step there);
+//           a smaller entry is carried to within 2^-21.8 of the row's largest magnitude.
 //   values  O^T[dv][n]  += sum_key code[key][dv] * Pt[n][key] tcgen05 kind::f8f6f4,
 //           M = 128 dv (x4 chunks), N = rows, K = keys; the same FP8 tile read MN-major
-//           The probabilities (scaled by 2^8) are split into three e4m3 terms, which
-//           carries 12 significant bits, about what fp16 would.
+//           (A: e4m3 codes) against the probabilities as three e5m2 terms (B). A weight
+//           p = 2^(x - m + 11) (at most 2^15) is rounded to fp16 and split by round to
+//           nearest into e5m2 terms t0 + t1 + t2: each term takes the leading 3 bits of
+//           what the previous ones left, so the sum carries p to about fp16's precision,
+//           and e5m2's range (2^-16 .. 57344) keeps that precision for weights down to
+//           about 2^-19 of the running maximum. Smaller weights lose bits gradually; the
+//           smallest one kept is 2^-28 of the maximum. (An e4m3 split loses every weight
+//           below about 2^-14 of the maximum: a long tail under a dominant key would then
+//           vanish from the numerator but not from the row sum.)
 // Keys sit on the MMA's M side ("swap A/B"): 8-16 heads x 1-4 positions are far below
 // M = 128, so the few query rows take the narrow N side and nothing is padded in memory.
 // Softmax is online over key tiles; one warpgroup owns one key per thread (its TMEM
@@ -47,8 +60,9 @@ constexpr int kMaxThreads = 512;  // producer, 2 MMA issuers, query stager, 2-3 
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kPScale = 4.0f;      // P carried as 2^(x - m + 4): at most 2^8 while x <= m + 4
+constexpr float kPScale = 11.0f;     // P carried as 2^(x - m + 11): at most 2^15 while x <= m + 4
 constexpr float kRescaleGap = 4.0f;  // the running max (log2 units) moves only past m + 4
+constexpr float kQTerm2 = 16.0f;     // the second query term carries the residual times 16
 constexpr int kPrefetchTiles = 1;    // tiles the producer pulls into L2 ahead of its TMA loads
 
 template <int RP>
@@ -80,7 +94,7 @@ struct Cfg {
   static constexpr int kQB = (RP == 16) ? 2 : 1;
   // A stage holds one key tile: dims 0..511 as four SW128 chunks of 128 keys x 128 bytes,
   // then dims 512..575 (the tail, SW64, 128 keys x 64 bytes). At 48 rows each stage also
-  // holds its tile's probabilities (P^T, three e4m3 terms of 6 KB), so the softmax can
+  // holds its tile's probabilities (P^T, three e5m2 terms of 6 KB), so the softmax can
   // write the next tile's P while the values MMA still reads this one: terms 1 and 2 in
   // 12 KB between the chunks and the tail, term 0 over the first 6 KB of the tail, which
   // the scores no longer need by then. Otherwise one P buffer serves every tile.
@@ -304,14 +318,14 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
   return h;
 }
-__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+__device__ __forceinline__ uint32_t f16x2_to_e5m2x2(uint32_t h) {
   uint16_t c;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(c) : "r"(h));
+  asm("cvt.rn.satfinite.e5m2x2.f16x2 %0, %1;" : "=h"(c) : "r"(h));
   return c;
 }
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c) {
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t c) {
   uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)c));
+  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h) : "h"((uint16_t)c));
   return h;
 }
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
@@ -333,8 +347,10 @@ __device__ __forceinline__ int q_offset(int n, int w16) {
 }
 
 // Stage rows w, w + nw, ... (< RP) of one unit's queries into a query operand buffer as two
-// e4m3 terms (a per-row power-of-two scale makes the split exact for bf16), and the rows'
-// score scales into row_scale[]. Rows at or past R are written as zeros.
+// e4m3 terms after a per-row power-of-two scale (the entry rounded, then 16 x the residual
+// rounded: exact for entries down to 2^-14.8 of the row's largest magnitude, within
+// 2^-21.8 of it below), and the rows' score scales into row_scale[]. Rows at or past R are
+// written as zeros.
 template <int RP>
 __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int* row_off,
                                        const uint16_t* qseq, uint8_t* qdst, float* row_scale,
@@ -399,7 +415,7 @@ __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int
           const float a0 = x[e] * up, a1 = x[e + 1] * up;
           const uint16_t c1 = to_e4m3x2(a0, a1);
           const float2 b1 = from_e4m3x2(c1);
-          const uint16_t c2 = to_e4m3x2(a0 - b1.x, a1 - b1.y);
+          const uint16_t c2 = to_e4m3x2((a0 - b1.x) * kQTerm2, (a1 - b1.y) * kQTerm2);
           const int wi = e >> 2, sh = (e & 2) * 8;
           if ((e & 2) == 0) {
             t1w[wi] = c1;
@@ -432,6 +448,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   uint8_t* pbuf = smem + C::kOffP;
   uint8_t* qbuf = smem + C::kOffQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // profiling hook: this CTA's stamps, or null
+  unsigned long long* const trace =
+      (p.trace && (int)blockIdx.x < p.trace_ctas) ? p.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
+  if (trace && threadIdx.x == 0) trace[kTrEntry] = globaltimer_ns();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -479,6 +499,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   // dependent of this one, may be scheduled from here on and waits for this grid itself.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
+  if (trace && threadIdx.x == 0) trace[kTrWaited] = globaltimer_ns();
 
   if (!args.prefill) {
     // ---- split plan (decode/verify), computed by every CTA for itself. All sequences,
@@ -561,6 +582,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     }
     __syncthreads();
   }
+  if (trace && threadIdx.x == 0) trace[kTrPlanned] = globaltimer_ns();
 
   // The first unit's queries are on every CTA's critical path: warps 2.. stage them into
   // shared memory together (about two rows each). Later units' rows go to this CTA's query
@@ -714,8 +736,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // PV of every tile the moment its probabilities are in shared memory; completion hands
     // the KV stage back to the producer and lets the softmax reuse P and rescale O.
     if (lane == 0) {
-      constexpr uint32_t idesc_stacked = instr_desc(0, 0, 1, 1, 128, 3 * RP);
-      constexpr uint32_t idesc_term = instr_desc(0, 0, 1, 1, 128, RP);
+      // A = V^T as e4m3 codes, B = P^T as e5m2 terms (kind::f8f6f4 takes each operand's
+      // format from its own descriptor field), both MN-major
+      constexpr uint32_t idesc_stacked = instr_desc(kFmtE4M3, kFmtE5M2, 1, 1, 128, 3 * RP);
+      constexpr uint32_t idesc_term = instr_desc(kFmtE4M3, kFmtE5M2, 1, 1, 128, RP);
       const uint64_t a0 = smem_desc(smem_addr(smem + C::kOffStages), kChunkBytes, 1024, Swizzle::k128B);
       // P^T of stage 0's tile (at 48 rows; each stage has its own) or the shared buffer
       const uint64_t b0 = smem_desc(smem_addr(C::kPInStage ? smem + C::kOffStages + 4 * kChunkBytes : pbuf),
@@ -870,11 +894,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             tmem_ld8(base + RP + c, b2);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[c + e] = (a[e] + b2[e]) * rs[c + e];
+            for (int e = 0; e < 8; ++e) x[c + e] = fmaf(b2[e], 1.0f / kQTerm2, a[e]) * rs[c + e];
           }
         }
         tc_fence_before();
         mbar_arrive(&ms->s_empty[sb]);
+        if (trace && tile == 0 && threadIdx.x == 32 * kSoftmaxWarp0) trace[kTrFirstScores] = globaltimer_ns();
         // masking only on tiles that reach past the first new position's last visible key
         if (k0 + kTileKeys - 1 > lim0) {
 #pragma unroll
@@ -921,7 +946,9 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
 #pragma unroll
         for (int r = 0; r < RH; ++r) moff[r] = (m[r] == -INFINITY) ? 0.f : m[r] - kPScale;
-        // p = 2^(x - m + 4) <= 2^8 rounded to fp16, carried exactly by three e4m3 terms
+        // p = 2^(x - m + 11) <= 2^15 rounded to fp16, then three e5m2 terms, each the
+        // nearest e5m2 value to what the terms before it left (the differences are exact
+        // in fp16); the row sum takes the float32 p
         uint32_t w1[RH / 4], w2[RH / 4], w3[RH / 4];
 #pragma unroll
         for (int r = 0; r < RH; r += 2) {
@@ -930,11 +957,11 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           l[r] += p0;
           l[r + 1] += p1;
           const uint32_t h = f32x2_to_f16x2(p0, p1);
-          const uint32_t c1 = f16x2_to_e4m3x2(h);
-          const uint32_t r1 = hsub2(h, e4m3x2_to_f16x2(c1));
-          const uint32_t c2 = f16x2_to_e4m3x2(r1);
-          const uint32_t r2 = hsub2(r1, e4m3x2_to_f16x2(c2));
-          const uint32_t c3 = f16x2_to_e4m3x2(r2);
+          const uint32_t c1 = f16x2_to_e5m2x2(h);
+          const uint32_t r1 = hsub2(h, e5m2x2_to_f16x2(c1));
+          const uint32_t c2 = f16x2_to_e5m2x2(r1);
+          const uint32_t r2 = hsub2(r1, e5m2x2_to_f16x2(c2));
+          const uint32_t c3 = f16x2_to_e5m2x2(r2);
           const int wi = r >> 2;
           if ((r & 2) == 0) {
             w1[wi] = c1;
@@ -1004,6 +1031,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         mbar_arrive(&ms->p_full[tile & 1]);
       }
       if (!ok) break;
+      if (trace && threadIdx.x == 32 * kSoftmaxWarp0) trace[kTrLastP] = globaltimer_ns();
       // ---- epilogue: row sums, then O / l
 #pragma unroll
       for (int r = 0; r < RH; ++r) {
@@ -1071,6 +1099,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
       }
       ++k;
+      if (trace && threadIdx.x == 32 * kSoftmaxWarp0) {
+        trace[kTrEpilogue] = globaltimer_ns();
+        trace[kTrCounts] = ((unsigned long long)tile << 32) | k;
+      }
     }
   }
 
@@ -1080,6 +1112,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (trace && threadIdx.x == 0) trace[kTrExit] = globaltimer_ns();
   if (threadIdx.x == 0) {
     // this CTA's status word (a later launch of the same call only adds errors)
     if (args.status_overwrite || ms->status != 0) p.status[blockIdx.x] = ms->status;

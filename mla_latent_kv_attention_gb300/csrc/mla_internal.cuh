@@ -113,7 +113,17 @@ struct AttnParams {
   int num_ctas;
   int test_stall;     // test hook: the producer issues no loads, so every consumer's bounded
                       // wait runs out and the call reports MLA_ERR_TIMEOUT
+  unsigned long long* trace;  // profiling hook: kTraceWords globaltimer stamps per CTA, or null
+  int trace_ctas;             // CTAs the trace buffer has room for
 };
+
+// Per-CTA stamps of the profiling hook (mla_set_trace_buffer), in nanoseconds of the GPU's
+// global timer: entry, end of the wait on the previous kernel, end of the split plan, the
+// first tile's scores read by the softmax, the last tile's probabilities written, end of
+// the last epilogue, exit; then the tiles and units the CTA processed.
+constexpr int kTraceWords = 8;
+enum TraceSlot { kTrEntry = 0, kTrWaited, kTrPlanned, kTrFirstScores, kTrLastP, kTrEpilogue,
+                 kTrExit, kTrCounts };
 
 // The CTA of a split plan that holds block x, when `total` blocks are cut into n ranges
 // [c * total / n, (c + 1) * total / n): the largest c whose range starts at or before x.
@@ -185,6 +195,8 @@ cudaError_t launch_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t
                                 const int64_t* slots, int64_t n, float inv, unsigned* status,
                                 int num_sms, cudaStream_t s);
 cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches);
+cudaError_t launch_mha_projection(const void* latent, const void* w, void* kvup, int L, int N,
+                                  float kv_scale, unsigned* status, cudaStream_t s);
 cudaError_t launch_top_k_renorm(const float* probs, float* out, int B, int V, const int32_t* top_k,
                                 int k_all, cudaStream_t s);
 

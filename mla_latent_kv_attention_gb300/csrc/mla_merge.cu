@@ -98,6 +98,7 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
   float sum = 0.f;
   for (int i = lane + 32 * kLse; i < count; i += 32) {  // online, past 256 pieces
     const float x = __ldg(pl + slot_of(i) * R + r);
+    if (x == -INFINITY) continue;  // an empty partial adds nothing (and -inf - -inf is NaN)
     if (x > m) {
       sum = sum * expf(m - x);
       m = x;

@@ -12,7 +12,7 @@
 // Three steps:
 //   1. mha_dequant_kernel: cached rows -> latent [L][512] bf16 (e4m3 values, exact; the
 //      scale goes into the GEMM) and RoPE rows [L][64] bf16 (scaled).
-//   2. cuBLAS GEMM (a plain library GEMM): kvup [L][H][256] = kv_scale * latent @ W_ukv.
+//   2. mha_proj_kernel (mla_mha_proj.cu, tcgen05): kvup [L][H][256] = kv_scale * latent @ W_ukv.
 //   3. mha_attn_kernel: flash attention on tcgen05. One persistent CTA per SM walks units
 //      of (128 new positions, one head), longest first. Per 128-key tile: S = Q K^T
 //      (M = 128 queries, N = 128 keys, K = 192; twelve kind::f16 MMAs) into the TMEM score
@@ -23,7 +23,6 @@
 //      scores they came from; O_parity += P V with P read from TMEM (A operand) and V from
 //      shared memory (MN-major). Lazy rescale: an O is rescaled only when its row maximum
 //      grows by more than 2^8.
-#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -104,10 +103,11 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Mi
   return false;
 }
 
-// Units: a pair of adjacent query tiles (2i, 2i+1) of one head, taken by the two CTAs of a
-// cluster (rank 0 the later tile, rank 1 the earlier), which stream the same key and value
-// tiles: each CTA loads half of every tile and multicasts it to both. The pair covers the
-// later tile's keys; for the earlier tile the extra last tile is fully masked. Pairs are
+// Units: a pair of adjacent query tiles (2i, 2i+1) of one head, taken by two neighbouring
+// CTAs 2c and 2c + 1 (rank 0 the later tile, rank 1 the earlier), which stream the same key
+// and value tiles, each into its own shared memory (the second read of a tile is served by
+// L2). The pair covers the later tile's keys; for the earlier tile the extra last tile is
+// fully masked. Pairs are
 // ordered longest first and dealt to the clusters in a snake: round r gives pair r*G + c to
 // cluster c for even r and to cluster G-1-c for odd r. With an odd number of query tiles
 // the last pair holds one tile, which rank 1 repeats without writing it.
@@ -215,17 +215,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   Misc* ms = reinterpret_cast<Misc*>(smem + kOffMisc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x / 2, c = blockIdx.x / 2;  // clusters of two CTAs
-  const int rank = (int)cluster_ctarank();
+  const int G = gridDim.x / 2, c = blockIdx.x / 2;  // pairs of neighbouring CTAs
+  const int rank = (int)(blockIdx.x & 1);
   const Split sp = split_of(p.L, p.T, p.H, G);
-  constexpr uint16_t kBoth = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ms->k_full[s], 1);
-      mbar_init(&ms->k_empty[s], 2);  // both CTAs' MMAs release a buffer both of them fill
+      mbar_init(&ms->k_empty[s], 1);
       mbar_init(&ms->v_full[s], 1);
-      mbar_init(&ms->v_empty[s], 2);
+      mbar_init(&ms->v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->s_full[i], 1);
@@ -246,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(&ms->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before anything is multicast to them
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
 
@@ -266,14 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g & 1;
           if (g >= 2 && !(ok = wait_or_abort(&ms->k_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* kb = smem + kOffK + s * kKBytes;
-          mbar_arrive_expect_tx(&ms->k_full[s], kKBytes);  // both halves land here
+          mbar_arrive_expect_tx(&ms->k_full[s], kKBytes);
           const int n0 = j * kBN;
-          if (rank == 0) {
-            tma_load_3d_mc(kb, &map_kv, 0, x.h, n0, &ms->k_full[s], kBoth);
-            tma_load_2d_mc(kb + 2 * kBox, &map_rope, 0, n0, &ms->k_full[s], kBoth);
-          } else {
-            tma_load_3d_mc(kb + kBox, &map_kv, 64, x.h, n0, &ms->k_full[s], kBoth);
-          }
+          tma_load_3d(kb, &map_kv, 0, x.h, n0, &ms->k_full[s]);
+          tma_load_3d(kb + kBox, &map_kv, 64, x.h, n0, &ms->k_full[s]);
+          tma_load_2d(kb + 2 * kBox, &map_rope, 0, n0, &ms->k_full[s]);
         }
         if (!ok) break;
         ++k;
@@ -293,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= 2 && !(ok = wait_or_abort(&ms->v_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* vb = smem + kOffV + s * kVBytes;
           mbar_arrive_expect_tx(&ms->v_full[s], kVBytes);
-          tma_load_3d_mc(vb + rank * kBox, &map_kv, 128 + 64 * rank, x.h, j * kBN, &ms->v_full[s], kBoth);
+          tma_load_3d(vb, &map_kv, 128, x.h, j * kBN, &ms->v_full[s]);
+          tma_load_3d(vb + kBox, &map_kv, 192, x.h, j * kBN, &ms->v_full[s]);
         }
       }
     }
@@ -319,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = smem_desc(v_addr + ks * 2048, kBox, 1024, Swizzle::k128B);
           mma_f16_tmem_a(ocol, pcol + ks * 8, b, idesc_pv, (first && ks == 0) ? 0u : 1u);
         }
-        mma_commit_mc(&ms->v_empty[gx & 1], kBoth);
+        mma_commit(&ms->v_empty[gx & 1]);
         mma_commit(&ms->pv_done[gx & 1]);
         return true;
       };
@@ -343,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(tmem + s * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&ms->s_full[s]);
-          mma_commit_mc(&ms->k_empty[s], kBoth);
+          mma_commit(&ms->k_empty[s]);
           if (j == n - 1) mma_commit(&ms->q_free);
           if (j >= 1 && !(ok = pv(g - 1, j <= 2))) break;
         }
@@ -520,9 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  // neither CTA leaves while the other may still multicast into it or release its buffers;
   // after an abort, give loads already in flight a moment to land
-  cluster_sync();
   if (ms->abort && threadIdx.x == 0) {
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 50000) {
@@ -644,17 +638,9 @@ static EncodeFn tensor_map_encoder() {
   return fn;
 }
 
-// One cuBLAS handle per thread and device (created on first use, kept for the process).
-static cublasHandle_t blas_handle(int dev) {
-  thread_local cublasHandle_t handles[64] = {};
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
-  return handles[dev];
-}
-
 cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches) {
   const int pairs = (((a.T + kBM - 1) / kBM) + 1) / 2 * a.H;
-  const int grid = 2 * std::min(num_sms / 2, pairs);  // clusters of two CTAs
+  const int grid = 2 * std::min(num_sms / 2, pairs);  // pairs of CTAs
   // 1. dequantise (its status word follows the attention CTAs' words and is cleared first)
   unsigned* dq_status = a.status + grid;
   cudaError_t e = cudaMemsetAsync(dq_status, 0, sizeof(unsigned), s);
@@ -667,15 +653,9 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*launches;
-  // 2. up-projection: kvup (column-major [H*256] x L) = W (column-major [H*256] x 512) x latent
-  cublasHandle_t h = blas_handle(a.device);
-  if (!h || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  const float alpha = a.kv_scale, beta = 0.f;
-  const int m = a.H * 256;
-  if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, m, a.L, kDV, &alpha, a.w_ukv, CUDA_R_16BF, m,
-                   a.latent, CUDA_R_16BF, kDV, &beta, a.kvup, CUDA_R_16BF, m, CUBLAS_COMPUTE_32F,
-                   CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorUnknown;
+  // 2. up-projection: kvup [L][H*256] = kv_scale * latent [L][512] @ w_ukv [512][H*256]
+  e = launch_mha_projection(a.latent, a.w_ukv, a.kvup, a.L, a.H * 256, a.kv_scale, dq_status, s);
+  if (e != cudaSuccess) return e;
   ++*launches;
   // 3. attention
   const EncodeFn encode = tensor_map_encoder();
@@ -729,13 +709,6 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, mha_attn_kernel, p, mq, mkv, mr);
   if (e == cudaSuccess) ++*launches;
   if (prof) cudaEventRecord(a.prof_stop, s);

@@ -110,23 +110,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Multicast forms: the box lands at the same shared-memory offset in every CTA of the
-// cluster named in `mask`, and each of them gets the bytes counted on its own barrier at
-// `bar`'s offset.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                               uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t mask) {
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -244,8 +233,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// Instruction descriptor: dense, D = f32, A/B type codes (kind::f8f6f4: e4m3 = 0;
-// kind::f16: f16 = 0, bf16 = 1), A/B major-ness (0 = K-major, 1 = MN-major), N and M.
+// Operand format codes of the instruction descriptor. kind::f8f6f4 takes A's and B's
+// formats independently; kind::f16 needs the same code on both (f16 = 0, bf16 = 1).
+constexpr uint32_t kFmtE4M3 = 0;  // kind::f8f6f4
+constexpr uint32_t kFmtE5M2 = 1;  // kind::f8f6f4
+
+// Instruction descriptor: dense, D = f32, A/B type codes (above), A/B major-ness
+// (0 = K-major, 1 = MN-major), N and M.
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_type, uint32_t b_type,
                                                   uint32_t a_mn_major, uint32_t b_mn_major,
                                                   uint32_t M, uint32_t N) {
@@ -279,15 +273,6 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on the barrier at `bar`'s offset in every CTA of the cluster named in `mask` once
-// every tcgen05 operation this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)), "h"(mask)
       : "memory");
 }
 

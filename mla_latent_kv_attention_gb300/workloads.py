@@ -17,9 +17,10 @@ Recipe (fixed draw order, one CPU ``torch.Generator`` seeded per workload):
   4. latent rows ``x ~ N(0, 1)`` in float32, one per logical cache slot (whole pages,
      so slots past ``seq_lens[b]`` in a sequence's last page hold valid codes too),
      quantised with one per-tensor scale ``kv_scale = amax / 448`` as
-     ``e4m3_rne(clamp(x / kv_scale, -448, 448))``. The clamp comes first because
-     ``x / kv_scale`` can round a hair above 448 and the float8 cast does not
-     saturate.
+     ``e4m3_rne(clamp(x * inv, -448, 448))``, ``inv = 1 / kv_scale`` and the product
+     both rounded to binary32 (the cache-append kernel quantises new rows the same
+     way). The clamp comes first because the product can round a hair above 448 and
+     the float8 cast does not saturate.
 ``sm_scale`` is ``1 / sqrt(192)`` for every workload.
 """
 from __future__ import annotations
@@ -75,8 +76,10 @@ class MlaInputs:
 
 
 def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
-    """float32 -> e4m3fn codes (uint8) with round-to-nearest-even after clamping."""
-    y = (x / scale).clamp_(-448.0, 448.0)
+    """float32 -> e4m3fn codes (uint8): x * (1 / scale), the reciprocal and the product
+    rounded to binary32, clamped to +-448, then rounded to nearest even."""
+    inv = torch.tensor(1.0, dtype=torch.float32) / torch.tensor(scale, dtype=torch.float32)
+    y = (x.float() * inv).clamp_(-448.0, 448.0)
     return y.to(torch.float8_e4m3fn).view(torch.uint8)
 
 
@@ -238,6 +241,94 @@ def mha_prefill(T: int = 8192, prefix: int = 32768, H: int = 12, seed: int = 0) 
     """The causal prefill chunk of the named workload (T new positions on a prefix) in the
     MHA form."""
     return mha_prefill_inputs(T, prefix, H, seed)
+
+
+# --- inputs with a wide dynamic range --------------------------------------------
+#
+# N(0, 1) queries and keys give scores that spread over about 1.7 nats, so almost every
+# weight sits within a few binades of its row's largest one. The inputs below reach the
+# cases that spread does not: one dominant key over a long, flat tail (an "attention
+# sink"), weights that fall off over tens of nats, and query rows whose entries span many
+# binades. They only set codes and query entries; the scores follow from the definition.
+
+E4M3_CODE_448 = 0x7E  # +448, the largest finite e4m3 value
+ROPE0 = DV            # first of the 64 RoPE dims (512..575)
+
+
+def _set_rope_block(inp: MlaInputs, b: int, positions: torch.Tensor, k: torch.Tensor) -> None:
+    """Rows `positions` of sequence b: RoPE dims 512 .. 512 + k - 1 hold +448, the rest of
+    the 64 RoPE dims hold 0 (k per position, 0..64)."""
+    pages = inp.page_table[b, (positions // inp.page_size).long()].long()
+    offs = (positions % inp.page_size).long()
+    dims = torch.arange(64)
+    block = torch.where(dims[None, :] < k[:, None], E4M3_CODE_448, 0).to(torch.uint8)
+    inp.pool[pages, offs, ROPE0:] = block
+
+
+def _ramp_query(inp: MlaInputs, nats_per_dim, spread) -> None:
+    """Queries whose score against a row with k RoPE dims at +448 (the rest 0) is
+    k x nats_per_dim[h] plus a random part: RoPE dims = nats_per_dim[h] / (448 kv_scale
+    sm_scale), dims 0..511 = spread[h] x (the N(0, 1) draw already there), rounded to bf16."""
+    H = inp.H
+    q = inp.q.float()
+    for h in range(H):
+        a = float(nats_per_dim[h]) / (448.0 * inp.kv_scale * inp.sm_scale)
+        q[:, :, h, ROPE0:] = a
+        q[:, :, h, :ROPE0] *= float(spread[h])
+    inp.q = q.to(torch.bfloat16)
+
+
+SINK_GAPS = (4.0, 6.0, 8.0, 10.0, 12.0, 16.0)
+
+
+def attention_sink(L: int = 142000, H: int = 12, n_q: int = 1, B: int = 1, seed: int = 0,
+                   sink_at: Optional[int] = None) -> MlaInputs:
+    """One key per sequence (position `sink_at`, default L // 3, visible to every new
+    position) stands about gap nats above a tail of L - 1 keys. Head h takes gap
+    SINK_GAPS[h % 6]; even heads have an exactly flat tail (every other key scores 0),
+    odd heads add the N(0, 1) query draw scaled by 1/2 on dims 0..511 (a tail spread of
+    about 0.9 nats). Values (dims 0..511) stay the usual N(0, 1) latent."""
+    inp = make_inputs(f"attention_sink_b{B}_h{H}_q{n_q}_l{L}", [L] * B, H=H, n_q=n_q, seed=seed)
+    at = L // 3 if sink_at is None else sink_at
+    pos = torch.arange(L)
+    for b in range(B):
+        _set_rope_block(inp, b, pos, torch.where(pos == at, 64, 0))
+    gaps = [SINK_GAPS[h % len(SINK_GAPS)] / 64.0 for h in range(H)]
+    _ramp_query(inp, gaps, [0.0 if h % 2 == 0 else 0.5 for h in range(H)])
+    return inp
+
+
+def graded_tail(L: int = 142000, H: int = 12, n_q: int = 1, nats: float = 30.0,
+                seed: int = 0) -> MlaInputs:
+    """Scores that fall off linearly over `nats` nats from the first key to the last, in
+    65 equal steps (key n has round(64 (1 - n / L)) RoPE dims at +448); even heads have no
+    other score component, odd heads add the N(0, 1) query draw scaled by 1/2."""
+    inp = make_inputs(f"graded_tail_h{H}_q{n_q}_l{L}", [L], H=H, n_q=n_q, seed=seed)
+    pos = torch.arange(L)
+    k = torch.round(64.0 * (1.0 - pos.double() / L)).long()
+    _set_rope_block(inp, 0, pos, k)
+    _ramp_query(inp, [nats / 64.0] * H, [0.0 if h % 2 == 0 else 0.5 for h in range(H)])
+    return inp
+
+
+def wide_range_query(lens: Sequence[int], H: int = 12, n_q: int = 1, binades: float = 20.0,
+                     big: Optional[float] = 4096.0, seed: int = 0) -> MlaInputs:
+    """Query rows whose entries span `binades` binades: |q_d| = 2^-u with u uniform in
+    [0, binades), random sign (bf16). With `big`, one entry of every odd row is set to
+    `big` (2^12 by default: all the row's other entries then sit below 2^-12 of it)."""
+    inp = make_inputs(f"wide_range_query_h{H}_q{n_q}", list(lens), H=H, n_q=n_q, seed=seed)
+    g = torch.Generator().manual_seed(seed + 7)
+    B = inp.B
+    u = torch.rand(B, n_q, H, D, generator=g, dtype=torch.float64) * binades
+    sign = torch.where(torch.rand(B, n_q, H, D, generator=g) < 0.5, -1.0, 1.0).double()
+    q = sign * torch.exp2(-u)
+    rows = q.view(-1, D)
+    at = torch.randint(0, D, (rows.shape[0],), generator=g)
+    if big is not None:
+        for r in range(1, rows.shape[0], 2):
+            rows[r, int(at[r])] = float(big)
+    inp.q = q.to(torch.bfloat16)
+    return inp
 
 
 WORKLOADS = {

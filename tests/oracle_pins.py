@@ -425,10 +425,36 @@ def pin_mha_sdpa(orc):
         np.testing.assert_allclose(l[i], lse[t, h], rtol=1e-14)
 
 
+def pin_attention_sink_closed_form(orc):
+    """A long row with one dominant key over a flat tail, in closed form: on the even heads
+    of the attention-sink input (query zero on dims 0..511, every RoPE dim equal to a), each
+    tail key scores exactly 0 and the sink s = sm_scale * 64 * a * 448 * kv_scale, so
+    lse = ln(L - 1 + e^s) and out = (sum of the tail's values + e^s v_sink) / (L - 1 + e^s).
+    Computed here from the codes with torch's float8 decode, in float64; causal verify rows
+    see the same keys up to their own position."""
+    L = 5000
+    for n_q in (1, 3):
+        inp = W.attention_sink(L=L, H=4, n_q=n_q, seed=11, sink_at=1234)
+        out, lse = orc.attention(inp)
+        codes = _gather_keys(inp, 0)
+        vals = codes.view(torch.float8_e4m3fn).double() * inp.kv_scale
+        for h in (0, 2):
+            a = inp.q[0, 0, h, W.ROPE0].double().item()
+            assert torch.all(inp.q[0, :, h, :W.ROPE0] == 0)
+            s = inp.sm_scale * 64 * a * 448.0 * inp.kv_scale
+            for j in range(n_q):
+                vis = L - n_q + j + 1
+                tail = vals[:vis, :DV].sum(0) - vals[1234, :DV]
+                den = (vis - 1) + math.exp(s)
+                want = (tail + math.exp(s) * vals[1234, :DV]) / den
+                assert abs(lse[0, j, h] - math.log(den)) < 1e-12 * max(1.0, abs(math.log(den)))
+                assert np.allclose(out[0, j, h], want.numpy(), rtol=1e-11, atol=1e-13)
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_bf16, pin_brute_force_sdpa, pin_constant_v, pin_single_key,
     pin_zero_query, pin_duplicate_key, pin_split_merge, pin_merge_weights, pin_permuted_pages,
     pin_head_padding_and_permutation, pin_causal_prefix, pin_sampled_rows, pin_e4m3_encode,
-    pin_cache_append, pin_top_k_renorm, pin_mha_absorbed_identity, pin_mha_zero_query,
+    pin_cache_append, pin_top_k_renorm, pin_attention_sink_closed_form, pin_mha_absorbed_identity, pin_mha_zero_query,
     pin_mha_sdpa,
 ]

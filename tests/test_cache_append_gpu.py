@@ -79,3 +79,21 @@ def test_append_then_verify():
                        inp.sm_scale, 64)
     ref_out, ref_lse = oracle.attention(inp2)
     compare(out, lse, ref_out, ref_lse, "verify after append")
+
+
+def test_append_reproduces_generator_codes():
+    """Rows appended through mla_cache_append hold exactly the codes the input generator
+    gives the same values (x * (1 / kv_scale) in binary32, clamped, rounded to nearest
+    even): appended rows and generated rows are indistinguishable to the attention
+    kernels."""
+    g = torch.Generator().manual_seed(71)
+    n = 4096
+    x = torch.randn(n, 576, generator=g).to(torch.bfloat16)
+    kv_scale = float(x.float().abs().max()) / 448.0
+    want = W.quantize_e4m3(x.float(), kv_scale)
+    pool_d = torch.zeros(n // 64, 64, 576, dtype=torch.uint8, device=DEV)
+    slots = torch.randperm(n, generator=g).to(torch.int64)
+    mla.mla_cache_append(pool_d, x.to(DEV), slots.to(DEV), kv_scale)
+    torch.cuda.synchronize()
+    got = pool_d.view(n, 576).cpu()[slots]
+    assert torch.equal(got, want)

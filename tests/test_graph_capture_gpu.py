@@ -46,7 +46,7 @@ def test_graph_replay_matches_eager():
 
     side = torch.cuda.Stream()
     with torch.cuda.stream(side):
-        calls()  # warm: the cuBLAS handle and module loading happen outside the capture
+        calls()  # warm: module loading and first-call set-up happen outside the capture
     torch.cuda.synchronize()
     eager = [t.clone() for t in (od, ld, ov, lv, om, lm, pool, tk)]
     for t in (od, ld, ov, lv, om, lm, tk):

@@ -138,15 +138,18 @@ def test_causal_prefill_small(T, prefix, H):
 
 def test_causal_prefill_full_sampled():
     """8,192 new positions on a 32,768-position prefix, 12 heads: every row is computed on
-    the GPU; the oracle checks the first and last positions, both sides of the boundary
-    between the prefix and the chunk, and random rows (rows are independent)."""
+    the GPU; the oracle checks every head of the first six positions (the first sits on
+    the boundary between the prefix and the chunk), the middle two, the last six (they
+    see all 40,960 keys) and twelve random positions (rows are independent)."""
     inp = W.causal_prefill()
     out, lse = run_prefill(inp)
     T, H = inp.n_q, inp.H
     g = np.random.default_rng(5)
-    pos = {0, 1, 2, 3, 4, 5, T // 2, T - 4, T - 3, T - 2, T - 1}
-    pos |= set(int(x) for x in g.integers(0, T, 40))
-    rows = np.array(sorted({(0, j, h) for j in pos for h in range(H)}), dtype=np.int32)[:300]
+    pos = [0, 1, 2, 3, 4, 5, T // 2 - 1, T // 2] + list(range(T - 6, T))
+    pos += [int(x) for x in g.choice(np.arange(6, T - 6), 12, replace=False)]
+    rows = np.array([(0, j, h) for j in pos for h in range(H)], dtype=np.int32)
+    assert len(rows) >= 256 and (rows[:, 1] == T - 1).any() and (rows[:, 1] == T // 2).any()
+    print(f"causal prefill: {len(rows)} sampled rows over positions {min(pos)}..{max(pos)}")
     ref_out, ref_lse = oracle.attention_rows(inp, rows)
     idx = (rows[:, 0], rows[:, 1], rows[:, 2])
     compare(out.cpu()[idx], lse.cpu()[idx], ref_out, ref_lse, "causal prefill (sampled rows)")

@@ -7,7 +7,9 @@ keeps in device memory. The test calls it through the C ABI twice in a row, on t
 different batches so the second call inherits the first call's leftovers in the shared
 workspace, and checks each result against mla_decode with a workspace of its own, within
 the tolerances every parity test here uses. It also checks that a batch too large for
-the fixed workspace is refused before any work is enqueued.
+the fixed workspace is refused before any work is enqueued, that its device-side status
+words (a page index outside the pool) are read through mla_read_status_static, and, once,
+that its result agrees with the float64 oracle.
 
 This file is named so that pytest collects it last.
 """
@@ -18,6 +20,7 @@ import pytest
 import torch
 
 import mla_latent_kv_attention_gb300 as mla
+import oracle
 from mla_latent_kv_attention_gb300 import workloads as W
 from tests.parity import compare
 
@@ -61,3 +64,21 @@ def test_static_workspace_rejects_too_large_batch():
     kv = mla.mla_kv_t(fake, 1, 64, fake, 1, fake, 1.0)
     status = lib.mla_decode_static_ws(ctypes.byref(kv), fake, B, 16, 0.1, fake, fake, None)
     assert status == 3  # MLA_ERR_WORKSPACE
+
+
+def test_static_workspace_status_and_oracle():
+    """A page index outside the pool is reported by mla_read_status_static (the kernel
+    reads no such page); the next call on the same fixed workspace is clean and agrees
+    with the oracle."""
+    lib = mla.library()
+    stream = torch.cuda.current_stream().cuda_stream
+    inp = W.make_inputs("nalloc_bad", [200, 700], H=12, n_q=1, seed=43)
+    kv = mla.KVCache.from_inputs(inp, "cuda")
+    kv.page_table[1, 2] = inp.pool.shape[0] + 5
+    _static_decode(inp, kv)
+    assert lib.mla_read_status_static(stream) == 6  # MLA_ERR_BOUNDS
+    kv.page_table[1, 2] = int(inp.page_table[1, 2])
+    out, lse = _static_decode(inp, kv)
+    assert lib.mla_read_status_static(stream) == 0
+    ref_out, ref_lse = oracle.attention(inp)
+    compare(out[:, None], lse[:, None], ref_out, ref_lse, "static workspace vs oracle")
