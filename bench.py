@@ -491,49 +491,57 @@ def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
                      "rows": n, "algorithmic_bytes": nbytes}
     del pool
     # decode-context parallelism over 8 ranks, played in turn on this GPU: every rank attends
-    # to its eighth of each sequence (float32 output + lse), then the 8 partials are merged.
+    # to its eighth of each sequence (float32 output + lse), then the partials are merged.
     # One step = the 8 ranks' calls + the merge; per rank = (step - merge) / 8, the
     # attention time of one rank of a real DCP8 group (the gather between GPUs excluded).
+    # With 4 verify positions a rank makes two calls (its final shards, causally masked, and
+    # its other shards seen whole by every position, each page read once).
     from mla_latent_kv_attention_gb300 import dcp
-    inp = W.batched_paged_decode()
-    kv = mla.KVCache.from_inputs(inp, dev)
-    q = inp.q.to(dev)
-    plan = dcp.shard_plan(inp.seq_lens.tolist(), inp.page_size, 8, 1)
-    views = [dcp.rank_views(kv, sh) for sh in plan]
-    po = torch.empty(8, inp.B, 1, inp.H, 512, dtype=torch.float32, device=dev)
-    pl = torch.empty(8, inp.B, 1, inp.H, dtype=torch.float32, device=dev)
-    wss = [mla.workspace(mla.MLA_OP_VERIFY, inp.B, inp.H, 1, dev) for _ in range(8)]
-    mout = torch.empty(inp.B * inp.H, 512, dtype=torch.bfloat16, device=dev)
-    mlse = torch.empty(inp.B * inp.H, dtype=torch.float32, device=dev)
+    for wname, inp in (("dcp8_batched_paged_decode", W.batched_paged_decode()),
+                       ("dcp8_spec_verify", W.spec_verify())):
+        kv = mla.KVCache.from_inputs(inp, dev)
+        q = inp.q.to(dev)
+        plan = dcp.shard_plan(inp.seq_lens.tolist(), inp.page_size, 8, inp.n_q)
+        views = [dcp.rank_views(kv, sh) for sh in plan]
+        P = plan[0].parts
+        po = torch.empty(8 * P, inp.B, inp.n_q, inp.H, 512, dtype=torch.float32, device=dev)
+        pl = torch.empty(8 * P, inp.B, inp.n_q, inp.H, dtype=torch.float32, device=dev)
+        wss = [mla.workspace(mla.MLA_OP_VERIFY, inp.B, inp.H, inp.n_q, dev) for _ in range(8 * P)]
+        rows = inp.B * inp.n_q * inp.H
+        mout = torch.empty(rows, 512, dtype=torch.bfloat16, device=dev)
+        mlse = torch.empty(rows, dtype=torch.float32, device=dev)
 
-    def ranks(i):
-        for r in range(8):
-            (view, rows), = views[r]
-            mla.mla_verify_f32(view, q, inp.sm_scale, out=po[r], lse=pl[r], ws=wss[r])
+        def ranks(i, views=views, q=q, po=po, pl=pl, wss=wss, inp=inp, P=P):
+            for r in range(8):
+                for k, (view, shift) in enumerate(views[r]):
+                    mla.mla_verify_f32(view, q, inp.sm_scale, out=po[r * P + k], lse=pl[r * P + k],
+                                       ws=wss[r * P + k], visible_shift=shift)
 
-    def step(i):
-        ranks(i)
-        mla.mla_merge_lse(po.view(8, -1, 512), pl.view(8, -1), out=mout, lse=mlse)
+        def step(i, ranks=ranks, po=po, pl=pl, mout=mout, mlse=mlse, P=P):
+            ranks(i)
+            mla.mla_merge_lse(po.view(8 * P, -1, 512), pl.view(8 * P, -1), out=mout, lse=mlse)
 
-    # device time: each form captured once in a CUDA graph and replayed (eagerly, the eight
-    # calls' host-side argument checks, not the GPU, set the pace)
-    side = torch.cuda.Stream()
-    with torch.cuda.stream(side):
-        step(0)
-    torch.cuda.synchronize()
-    graphs = {}
-    for name, fn in (("step", step), ("ranks", ranks)):
-        graphs[name] = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graphs[name]):
-            fn(0)
-    ms_step = _time_events(lambda i: graphs["step"].replay(), max(3, steps // 2), 3)
-    ms_ranks = _time_events(lambda i: graphs["ranks"].replay(), max(3, steps // 2), 3)
-    nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), 1, inp.H)
-    res["dcp8_batched_paged_decode"] = {
-        "us_per_step_8_ranks_one_gpu": ms_step * 1e3, "us_per_rank": ms_ranks * 1e3 / 8,
-        "us_merge": (ms_step - ms_ranks) * 1e3,
-        "GB_s_per_rank": nbytes / 8 / (ms_ranks / 8 / 1e3) / 1e9, "algorithmic_bytes": nbytes}
-    del kv, q, po, pl, wss, views, graphs
+        # device time: each form captured once in a CUDA graph and replayed (eagerly, the
+        # calls' host-side argument checks, not the GPU, set the pace)
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            step(0)
+        torch.cuda.synchronize()
+        graphs = {}
+        for name, fn in (("step", step), ("ranks", ranks)):
+            graphs[name] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graphs[name]):
+                fn(0)
+        ms_step = _time_events(lambda i: graphs["step"].replay(), max(3, steps // 2), 3)
+        ms_ranks = _time_events(lambda i: graphs["ranks"].replay(), max(3, steps // 2), 3)
+        nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), inp.n_q, inp.H)
+        gbs = nbytes / 8 / (ms_ranks / 8 / 1e3) / 1e9
+        res[wname] = {
+            "us_per_step_8_ranks_one_gpu": ms_step * 1e3, "us_per_rank": ms_ranks * 1e3 / 8,
+            "us_merge": (ms_step - ms_ranks) * 1e3, "GB_s_per_rank": gbs,
+            "frac_of_hbm_peak_per_rank": gbs / hbm_peak, "calls_per_rank": P,
+            "algorithmic_bytes": nbytes}
+        del kv, q, po, pl, wss, views, graphs
     # top-k renormalisation of the probability rows of a decode batch: 32 rows over a
     # 129,280-entry vocabulary, per-row k, sets rotated to exceed L2
     B, V = 32, 129280

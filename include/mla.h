@@ -135,6 +135,21 @@ mla_status_t mla_verify_f32(const mla_kv_t* kv, const void* q, int B, int n_q, i
                             size_t workspace_bytes, void* stream);
 
 /*
+ * mla_verify_f32 over one rank's shard of the positions, with the causal limit moved:
+ * key n of the view (0-based within it) is visible to new position j iff
+ * n <= seq_lens[b] - n_q + j + visible_shift. Under decode-context parallelism ("Scaling
+ * Kimi K3 ...", section "缓存可复用，还要能一致地恢复") the n_q new positions sit in the last
+ * shard of a sequence; every other shard lies wholly before them, so all of its keys are
+ * visible to all n_q positions: visible_shift >= n_q - 1 says so (values above n_q - 1
+ * act as n_q - 1), and each page of the shard is read once for the n_q positions
+ * together. visible_shift = 0 is mla_verify_f32. Negative: MLA_ERR_INVALID_ARG.
+ * Arguments, workspace and errors otherwise as mla_verify_f32.
+ */
+mla_status_t mla_verify_f32_shard(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
+                                  float sm_scale, int visible_shift, float* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Causal chunked prefill of one sequence: T new positions attend to the cached prefix
  * and causally to each other ("AMD MI355X推理Kimi K3：吞吐量超NVIDIA，首字优化显著",
  * section "首Token等待优化：简单补零解决大问题": long cold prefill through the MLA

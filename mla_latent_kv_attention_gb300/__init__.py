@@ -33,7 +33,7 @@ EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla
            "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append",
            "mla_top_k_renorm_prob", "mla_verify_f32", "mla_prefill_mha",
            "mla_prefill_mha_workspace_size", "mla_test_stall_next_call",
-           "mla_read_status_static", "mla_set_trace_buffer")
+           "mla_read_status_static", "mla_set_trace_buffer", "mla_verify_f32_shard")
 
 
 class MlaError(RuntimeError):
@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_verify.argtypes = [KV, P, i32, i32, i32, f32, P, P, P, sz, P]
     lib.mla_verify_f32.argtypes = [KV, P, i32, i32, i32, f32, P, P, P, sz, P]
     lib.mla_verify_f32.restype = i32
+    lib.mla_verify_f32_shard.argtypes = [KV, P, i32, i32, i32, f32, i32, P, P, P, sz, P]
+    lib.mla_verify_f32_shard.restype = i32
     lib.mla_prefill_mha_workspace_size.argtypes = [i32, i32, i32]
     lib.mla_prefill_mha_workspace_size.restype = sz
     lib.mla_prefill_mha.argtypes = [KV, i32, P, i32, i32, P, f32, P, P, P, sz, P]
@@ -226,8 +228,10 @@ def mla_prefill_mha(kv: KVCache, q: torch.Tensor, w_ukv: torch.Tensor, sm_scale:
 
 
 def mla_verify_f32(kv: KVCache, q: torch.Tensor, sm_scale: float, out=None, lse=None, ws=None,
-                   stream=None):
-    """As mla_verify with a float32 output [B, n_q, H, 512], for results merged later."""
+                   stream=None, visible_shift: int = 0):
+    """As mla_verify with a float32 output [B, n_q, H, 512], for results merged later.
+    visible_shift > 0 moves every new position's causal limit that many keys later
+    (mla_verify_f32_shard; n_q - 1 makes every key of the view visible to all of them)."""
     _q_check(q, 4)
     B, n_q, H = q.shape[0], q.shape[1], q.shape[2]
     out = torch.empty(B, n_q, H, MLA_DV, dtype=torch.float32, device=q.device) if out is None else out
@@ -236,9 +240,14 @@ def mla_verify_f32(kv: KVCache, q: torch.Tensor, sm_scale: float, out=None, lse=
     lse = torch.empty(B, n_q, H, dtype=torch.float32, device=q.device) if lse is None else lse
     ws = workspace(MLA_OP_VERIFY, B, H, n_q, q.device) if ws is None else ws
     c = kv.c_struct()
-    _check("mla_verify_f32", library().mla_verify_f32(
-        ctypes.byref(c), q.data_ptr(), B, n_q, H, sm_scale, out.data_ptr(), _ptr(lse),
-        ws.data_ptr(), ws.numel(), _stream(stream)))
+    if visible_shift == 0:
+        _check("mla_verify_f32", library().mla_verify_f32(
+            ctypes.byref(c), q.data_ptr(), B, n_q, H, sm_scale, out.data_ptr(), _ptr(lse),
+            ws.data_ptr(), ws.numel(), _stream(stream)))
+    else:
+        _check("mla_verify_f32_shard", library().mla_verify_f32_shard(
+            ctypes.byref(c), q.data_ptr(), B, n_q, H, sm_scale, int(visible_shift),
+            out.data_ptr(), _ptr(lse), ws.data_ptr(), ws.numel(), _stream(stream)))
     return out, lse
 
 

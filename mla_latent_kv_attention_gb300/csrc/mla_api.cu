@@ -76,7 +76,7 @@ thread_local int g_test_stall = 0;
 
 mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H, float sm_scale,
                        void* out, float* lse, void* ws, size_t ws_bytes, void* stream,
-                       bool out_is_f32 = false) {
+                       bool out_is_f32 = false, int mask_shift = 0) {
   g_last_launches = 0;
   mla_status_t st = check_kv(kv);
   if (st != MLA_OK) return st;
@@ -95,6 +95,7 @@ mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
   mla::AttnParams p = base_params(kv, q, B, n_q, H, sm_scale, out, lse);
   p.test_stall = g_test_stall;
   g_test_stall = 0;
+  p.mask_shift = mask_shift;
   if (out_is_f32) {
     p.out = nullptr;
     p.out_f32 = static_cast<float*>(out);
@@ -157,6 +158,15 @@ mla_status_t mla_verify_f32(const mla_kv_t* kv, const void* q, int B, int n_q, i
                             float sm_scale, float* out, float* lse, void* workspace,
                             size_t workspace_bytes, void* stream) {
   return run_split(kv, q, B, n_q, H, sm_scale, out, lse, workspace, workspace_bytes, stream, true);
+}
+
+mla_status_t mla_verify_f32_shard(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
+                                  float sm_scale, int visible_shift, float* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (visible_shift < 0) return MLA_ERR_INVALID_ARG;
+  const int shift = (n_q >= 1 && visible_shift > n_q - 1) ? n_q - 1 : visible_shift;
+  return run_split(kv, q, B, n_q, H, sm_scale, out, lse, workspace, workspace_bytes, stream, true,
+                   shift);
 }
 
 size_t mla_prefill_mha_workspace_size(int L, int H, int device) {

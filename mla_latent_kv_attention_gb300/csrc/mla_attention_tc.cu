@@ -865,9 +865,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         continue;
       }
       const int L = un.L;
-      // last visible key of new position j is L - n_q + j (and the unit ends at key_hi)
+      // last visible key of new position j is L - n_q + j + mask_shift (and the unit ends at
+      // key_hi); mask_shift is 0 except for a shard that holds none of the new positions
       const int lim_cap = un.key_hi - 1;
-      const int lim0 = min(lim_cap, L - p.n_q + un.j0);
+      const int lim0 = min(lim_cap, L - p.n_q + un.j0 + p.mask_shift);
       // this unit's row scales (staged with its query terms)
       if (!(ok = wait_or_abort(&ms->q_full[k % C::kQB], (k / C::kQB) & 1, ms, p))) break;
       float rs[RH], m[RH], l[RH];

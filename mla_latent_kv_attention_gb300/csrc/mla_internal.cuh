@@ -113,6 +113,7 @@ struct AttnParams {
   int num_ctas;
   int test_stall;     // test hook: the producer issues no loads, so every consumer's bounded
                       // wait runs out and the call reports MLA_ERR_TIMEOUT
+  int mask_shift;     // key n visible to new position j iff n <= L - n_q + j + mask_shift
   unsigned long long* trace;  // profiling hook: kTraceWords globaltimer stamps per CTA, or null
   int trace_ctas;             // CTAs the trace buffer has room for
 };

@@ -11,9 +11,11 @@ A rank's shard is a view of the shared page table (its pages, its shard length);
 the pool is copied. With n_q new positions (speculative verify) the new positions are the
 sequence's last n_q, so the shard that holds them (the final shard, made to hold at least
 n_q positions) is the only one a causal mask reaches. Every other shard is wholly visible
-to every new position and runs as n_q one-position queries. A rank therefore contributes
-two partials per row when n_q > 1 (the final-shard call and the whole-shard call); the one
-that does not apply to a sequence has no key, lse = -inf and weight 0 in the merge.
+to every new position: it runs with the causal limit moved past its end
+(``mla_verify_f32_shard``, visible_shift = n_q - 1), so its pages are read once for all n_q
+positions. A rank therefore contributes two partials per row when n_q > 1 (the final-shard
+call and the whole-shard call); the one that does not apply to a sequence has no key,
+lse = -inf and weight 0 in the merge.
 
 ``shard_plan`` and ``shard_views`` are host logic (``rank_views`` wraps the views as caches);
 ``rank_partials`` runs the rank's attention through ``mla_verify_f32``; ``gather_partials`` is the all-gather (in host memory
@@ -28,7 +30,7 @@ from typing import List, Optional, Sequence, Tuple
 import numpy as np
 import torch
 
-from . import MLA_D, MLA_DV, KVCache, mla_merge_lse, mla_verify_f32
+from . import MLA_DV, KVCache, mla_merge_lse, mla_verify_f32
 
 
 @dataclasses.dataclass
@@ -81,9 +83,10 @@ def shard_plan(seq_lens: Sequence[int], page_size: int, world: int, n_q: int = 1
 def shard_views(page_table: torch.Tensor, shard: Shard):
     """The rank's page-table views, on page_table's device.
 
-    Returns [(page_table, seq_lens, n_q), ...], one entry per partial: for n_q == 1 the
-    shard itself; for n_q > 1 first the final shards with n_q rows each (other sequences
-    empty), then every other shard as B * n_q one-row sequences (final ones empty)."""
+    Returns [(page_table, seq_lens, visible_shift), ...], one entry per partial, each over
+    the B sequences with n_q rows: for n_q == 1 the shard itself (shift 0); for n_q > 1
+    first the final shards, causally masked (shift 0, other sequences empty), then every
+    other shard seen whole by every new position (shift n_q - 1, final ones empty)."""
     dev = page_table.device
     B = page_table.shape[0]
     width = max(1, int(shard.num_pages.max()) if B else 1)
@@ -94,20 +97,19 @@ def shard_views(page_table: torch.Tensor, shard: Shard):
     pt = torch.where(used, torch.gather(page_table.cpu().to(torch.int64), 1, idx),
                      torch.full_like(idx, -1)).to(torch.int32)
     length = torch.from_numpy(shard.length).to(torch.int32)
+    pt = pt.contiguous().to(dev)
     if shard.n_q == 1:
-        return [(pt.contiguous().to(dev), length.to(dev), 1)]
+        return [(pt, length.to(dev), 0)]
     final = torch.from_numpy(shard.final)
     lens_final = torch.where(final, length, torch.zeros_like(length))
     lens_rest = torch.where(final, torch.zeros_like(length), length)
-    return [(pt.contiguous().to(dev), lens_final.to(dev), shard.n_q),
-            (pt.repeat_interleave(shard.n_q, dim=0).contiguous().to(dev),
-             lens_rest.repeat_interleave(shard.n_q).to(dev), 1)]
+    return [(pt, lens_final.to(dev), 0), (pt, lens_rest.to(dev), shard.n_q - 1)]
 
 
 def rank_views(kv: KVCache, shard: Shard):
-    """The rank's attention calls as [(KVCache view, rows per sequence)], on kv's device."""
-    return [(KVCache(kv.pool, pt, lens, kv.kv_scale), rows)
-            for pt, lens, rows in shard_views(kv.page_table, shard)]
+    """The rank's attention calls as [(KVCache view, visible_shift)], on kv's device."""
+    return [(KVCache(kv.pool, pt, lens, kv.kv_scale), shift)
+            for pt, lens, shift in shard_views(kv.page_table, shard)]
 
 
 def rank_partials(views, q: torch.Tensor, sm_scale: float,
@@ -123,13 +125,11 @@ def rank_partials(views, q: torch.Tensor, sm_scale: float,
         part_out = torch.empty(P, B, n_q, H, MLA_DV, dtype=torch.float32, device=q.device)
     if part_lse is None:
         part_lse = torch.empty(P, B, n_q, H, dtype=torch.float32, device=q.device)
-    for i, (view, rows) in enumerate(views):
-        qi = q if rows == n_q else q.reshape(B * n_q, 1, H, MLA_D)
-        if view.seq_lens.shape[0] != qi.shape[0]:
+    for i, (view, shift) in enumerate(views):
+        if view.seq_lens.shape[0] != B:
             raise ValueError("views do not match q's batch")
-        oi = part_out[i].view(qi.shape[0], rows, H, MLA_DV)
-        li = part_lse[i].view(qi.shape[0], rows, H)
-        mla_verify_f32(view, qi, sm_scale, out=oi, lse=li, stream=stream)
+        mla_verify_f32(view, q, sm_scale, out=part_out[i], lse=part_lse[i], stream=stream,
+                       visible_shift=shift)
     return part_out, part_lse
 
 

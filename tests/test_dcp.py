@@ -46,15 +46,22 @@ def test_shard_plan_covers_each_sequence(world, n_q):
             assert finals == (1 if L > 0 else 0)
 
 
-def _view_inputs(inp, pt, lens, rows):
-    q = inp.q if rows == inp.n_q else inp.q.reshape(inp.B * inp.n_q, 1, inp.H, inp.q.shape[-1])
-    return dataclasses.replace(inp, page_table=pt, seq_lens=lens, q=q)
+def _view_inputs(inp, pt, lens, shift):
+    """The oracle's form of a view: causal as defined (shift 0), or, for a shard every new
+    position sees whole (shift n_q - 1), each new position as a one-position query over the
+    whole shard."""
+    if shift == 0:
+        return dataclasses.replace(inp, page_table=pt, seq_lens=lens)
+    assert shift == inp.n_q - 1
+    q = inp.q.reshape(inp.B * inp.n_q, 1, inp.H, inp.q.shape[-1])
+    return dataclasses.replace(inp, page_table=pt.repeat_interleave(inp.n_q, dim=0),
+                               seq_lens=lens.repeat_interleave(inp.n_q), q=q)
 
 
 def _oracle_partials(inp, shard):
     outs, lses = [], []
-    for pt, lens, rows in dcp.shard_views(inp.page_table, shard):
-        o, l = oracle.attention(_view_inputs(inp, pt, lens, rows))
+    for pt, lens, shift in dcp.shard_views(inp.page_table, shard):
+        o, l = oracle.attention(_view_inputs(inp, pt, lens, shift))
         outs.append(o.reshape(inp.B, inp.n_q, inp.H, -1))
         lses.append(l.reshape(inp.B, inp.n_q, inp.H))
     return np.stack(outs), np.stack(lses)

@@ -64,3 +64,26 @@ def test_dcp_harness_named_workloads(name, world):
     torch.cuda.synchronize()
     ref_out, ref_lse = oracle.attention(inp)
     compare(out, lse, ref_out, ref_lse, f"dcp {name} world {world}")
+
+
+@pytest.mark.parametrize("lens,H,n_q", [([2000, 4, 257, 0], 12, 4), ([513, 77], 16, 2),
+                                        ([20000] * 2, 12, 3)])
+def test_verify_f32_shard_sees_whole_view(lens, H, n_q):
+    """visible_shift = n_q - 1: every new position sees every key of the view, as n_q
+    one-position queries over it would (the oracle computes it that way); shift 0 is
+    mla_verify_f32 bit for bit."""
+    import dataclasses
+    inp = W.make_inputs("shard", lens, H=H, n_q=n_q, seed=sum(lens) + n_q)
+    kv = mla.KVCache.from_inputs(inp, DEV)
+    q = inp.q.to(DEV)
+    out, lse = mla.mla_verify_f32(kv, q, inp.sm_scale, visible_shift=n_q - 1)
+    out0, lse0 = mla.mla_verify_f32(kv, q, inp.sm_scale, visible_shift=0)
+    ref0, rl0 = mla.mla_verify_f32(kv, q, inp.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out0, ref0) and torch.equal(lse0, rl0)
+    one = dataclasses.replace(inp, page_table=inp.page_table.repeat_interleave(n_q, dim=0),
+                              seq_lens=inp.seq_lens.repeat_interleave(n_q),
+                              q=inp.q.reshape(inp.B * n_q, 1, H, 576))
+    ref_out, ref_lse = oracle.attention(one)
+    compare(out.reshape(ref_out.shape), lse.reshape(ref_lse.shape), ref_out, ref_lse,
+            f"whole-view verify n_q={n_q}")
