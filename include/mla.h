@@ -275,11 +275,13 @@ void mla_set_profile_events(void* start, void* stop);
 /*
  * Profiling hook. With a device buffer of `bytes` (8-byte aligned), the next decode /
  * verify / prefill calls on this host thread make each CTA c of their attention kernel
- * (while c < bytes / 64) write eight 64-bit words at buffer + 64 c: the GPU's global timer
- * (ns) at entry, after the wait on the previous kernel, after the split plan, when the
- * first tile's scores were read, when the last tile's probabilities were written, after
- * its last epilogue and at exit, then (tiles << 32 | units) it processed. NULL switches it
- * off. The buffer stays owned by the caller; the results are undefined while two calls
+ * (while c < bytes / 128) write sixteen 64-bit words at buffer + 128 c: the GPU's global
+ * timer (ns) at entry, after the wait on the previous kernel, after the split plan, when
+ * the first tile's scores were read, when the last tile's probabilities were written, when
+ * the last values MMA completed, after its last epilogue and at exit; then (tiles << 32 |
+ * units) it processed; then, for CTAs with two units or more, the end of the first unit's
+ * epilogue and the second unit's first scores (words 11-15 are not written). NULL switches
+ * it off. The buffer stays owned by the caller; the results are undefined while two calls
  * overlap on the GPU.
  */
 void mla_set_trace_buffer(void* device_buffer, size_t bytes);

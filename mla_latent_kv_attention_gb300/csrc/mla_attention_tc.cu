@@ -900,7 +900,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&ms->s_empty[sb]);
-        if (trace && tile == 0 && threadIdx.x == 32 * kSoftmaxWarp0) trace[kTrFirstScores] = globaltimer_ns();
+        if (trace && threadIdx.x == 32 * kSoftmaxWarp0 && t == 0) {
+          if (tile == 0) trace[kTrFirstScores] = globaltimer_ns();
+          if (k == 1) trace[kTrUnit2Scores] = globaltimer_ns();
+        }
         // masking only on tiles that reach past the first new position's last visible key
         if (k0 + kTileKeys - 1 > lim0) {
 #pragma unroll
@@ -1051,6 +1054,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       }
       if (!(ok = wait_pv_upto((int)tile - 1))) break;
       tc_fence_after();
+      if (trace && threadIdx.x == 32 * kSoftmaxWarp0) trace[kTrLastPV] = globaltimer_ns();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int NT = C::oterms(c);
@@ -1103,6 +1107,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       if (trace && threadIdx.x == 32 * kSoftmaxWarp0) {
         trace[kTrEpilogue] = globaltimer_ns();
         trace[kTrCounts] = ((unsigned long long)tile << 32) | k;
+        if (k == 1) trace[kTrUnit1End] = globaltimer_ns();
       }
     }
   }

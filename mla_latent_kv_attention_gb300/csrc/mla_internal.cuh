@@ -120,11 +120,13 @@ struct AttnParams {
 
 // Per-CTA stamps of the profiling hook (mla_set_trace_buffer), in nanoseconds of the GPU's
 // global timer: entry, end of the wait on the previous kernel, end of the split plan, the
-// first tile's scores read by the softmax, the last tile's probabilities written, end of
-// the last epilogue, exit; then the tiles and units the CTA processed.
-constexpr int kTraceWords = 8;
-enum TraceSlot { kTrEntry = 0, kTrWaited, kTrPlanned, kTrFirstScores, kTrLastP, kTrEpilogue,
-                 kTrExit, kTrCounts };
+// first tile's scores read by the softmax, the last tile's probabilities written, the last
+// values MMA done, end of the last epilogue, exit; the tiles and units the CTA processed;
+// end of the first unit's epilogue and the second unit's first scores (CTAs with two units
+// or more).
+constexpr int kTraceWords = 16;
+enum TraceSlot { kTrEntry = 0, kTrWaited, kTrPlanned, kTrFirstScores, kTrLastP, kTrLastPV,
+                 kTrEpilogue, kTrExit, kTrCounts, kTrUnit1End, kTrUnit2Scores };
 
 // The CTA of a split plan that holds block x, when `total` blocks are cut into n ranges
 // [c * total / n, (c + 1) * total / n): the largest c whose range starts at or before x.
