@@ -440,31 +440,34 @@ def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
     out = torch.empty(m.T, m.H, 128, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(m.T, m.H, dtype=torch.float32, device=dev)
 
-    def mha_call(i):
-        mla.mla_prefill_mha(kv, q, w, m.cache.sm_scale, L=L, out=out, lse=lse, ws=ws)
+    for key, bf in (("mha_prefill", False), ("mha_prefill_bf16", True)):
+        def mha_call(i, bf=bf):
+            mla.mla_prefill_mha(kv, q, w, m.cache.sm_scale, L=L, out=out, lse=lse, ws=ws, bf16=bf)
 
-    ms = _time_events(mha_call, max(3, steps // 5), 2)
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record()
-    k1.record()
-    kms = []
-    for _ in range(3):
-        mla.mla_set_profile_events(k0, k1)
-        mha_call(0)
-        mla.mla_set_profile_events(None, None)
-        torch.cuda.synchronize()
-        kms.append(k0.elapsed_time(k1))
-    kms = sorted(kms)[1]
-    aflops = accounting.mha_attention_flops(m.T, L, m.H)
-    pflops = accounting.mha_projection_flops(L, m.H)
-    res["mha_prefill"] = {"ms_per_chunk": ms, "tok_s": m.T / (ms / 1e3),
-                          "attn_kernel_ms": kms, "attn_TFLOP_s": aflops / (kms / 1e3) / 1e12,
-                          "attn_frac_of_bf16_peak": aflops / (kms / 1e3) / 1e12 / bf16_peak,
-                          "attn_frac_of_bf16_sustained_peak":
-                              aflops / (kms / 1e3) / 1e12 / sustained_bf16_peak(),
-                          "whole_call_TFLOP_s": (aflops + pflops) / (ms / 1e3) / 1e12,
-                          "attention_flops": aflops, "projection_flops": pflops,
-                          "T": m.T, "prefix": L - m.T, "H": m.H}
+        ms = _time_events(mha_call, max(3, steps // 5), 2)
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record()
+        k1.record()
+        kms = []
+        for _ in range(3):
+            mla.mla_set_profile_events(k0, k1)
+            mha_call(0)
+            mla.mla_set_profile_events(None, None)
+            torch.cuda.synchronize()
+            kms.append(k0.elapsed_time(k1))
+        kms = sorted(kms)[1]
+        aflops = accounting.mha_attention_flops(m.T, L, m.H)
+        pflops = accounting.mha_projection_flops(L, m.H)
+        res[key] = {"ms_per_chunk": ms, "tok_s": m.T / (ms / 1e3),
+                    "attn_kernel_ms": kms, "attn_TFLOP_s": aflops / (kms / 1e3) / 1e12,
+                    "attn_frac_of_bf16_peak": aflops / (kms / 1e3) / 1e12 / bf16_peak,
+                    "attn_frac_of_bf16_sustained_peak":
+                        aflops / (kms / 1e3) / 1e12 / sustained_bf16_peak(),
+                    "whole_call_TFLOP_s": (aflops + pflops) / (ms / 1e3) / 1e12,
+                    "attention_flops": aflops, "projection_flops": pflops,
+                    "operands": ("bf16 keys, values, probabilities" if bf else
+                                 "keys as bf16 hi + lo, exact RoPE, fp16 values and probabilities"),
+                    "T": m.T, "prefix": L - m.T, "H": m.H}
     del kv, q, w, ws, out, lse
     # appending new rows to the cache: a prefill chunk's 8,192 rows and a decode step's 32,
     # into a pool larger than L2 (each call writes a different set of slots)

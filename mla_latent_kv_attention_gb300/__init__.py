@@ -33,7 +33,8 @@ EXPORTS = ("mla_workspace_size", "mla_decode", "mla_verify", "mla_prefill", "mla
            "mla_set_profile_events", "mla_decode_static_ws", "mla_cache_append",
            "mla_top_k_renorm_prob", "mla_verify_f32", "mla_prefill_mha",
            "mla_prefill_mha_workspace_size", "mla_test_stall_next_call",
-           "mla_read_status_static", "mla_set_trace_buffer", "mla_verify_f32_shard")
+           "mla_read_status_static", "mla_set_trace_buffer", "mla_verify_f32_shard",
+           "mla_prefill_mha_bf16")
 
 
 class MlaError(RuntimeError):
@@ -70,6 +71,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_prefill_mha_workspace_size.restype = sz
     lib.mla_prefill_mha.argtypes = [KV, i32, P, i32, i32, P, f32, P, P, P, sz, P]
     lib.mla_prefill_mha.restype = i32
+    lib.mla_prefill_mha_bf16.argtypes = [KV, i32, P, i32, i32, P, f32, P, P, P, sz, P]
+    lib.mla_prefill_mha_bf16.restype = i32
     lib.mla_test_stall_next_call.argtypes = []
     lib.mla_test_stall_next_call.restype = None
     lib.mla_prefill.argtypes = [KV, P, i32, i32, f32, P, P, P, sz, P]
@@ -202,10 +205,12 @@ def mla_verify(kv: KVCache, q: torch.Tensor, sm_scale: float, out=None, lse=None
 
 
 def mla_prefill_mha(kv: KVCache, q: torch.Tensor, w_ukv: torch.Tensor, sm_scale: float,
-                    L: Optional[int] = None, out=None, lse=None, ws=None, stream=None):
+                    L: Optional[int] = None, out=None, lse=None, ws=None, stream=None,
+                    bf16: bool = False):
     """MHA-form causal prefill of sequence 0: q [T, H, 192] bf16, w_ukv [512, H, 256] bf16
     -> (out [T, H, 128] bf16, lse [T, H] fp32). L (cached positions incl. the T new ones)
-    defaults to kv.seq_lens[0]."""
+    defaults to kv.seq_lens[0]. bf16=True calls mla_prefill_mha_bf16 (every tensor-core
+    operand in bf16: faster, looser)."""
     if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != 192 or not q.is_contiguous():
         raise ValueError("q must be a contiguous bfloat16 tensor [T, H, 192]")
     T, H = q.shape[0], q.shape[1]
@@ -221,7 +226,8 @@ def mla_prefill_mha(kv: KVCache, q: torch.Tensor, w_ukv: torch.Tensor, sm_scale:
             raise ValueError("no workspace size for these arguments")
         ws = torch.zeros(n, dtype=torch.uint8, device=q.device)
     c = kv.c_struct()
-    _check("mla_prefill_mha", library().mla_prefill_mha(
+    name = "mla_prefill_mha_bf16" if bf16 else "mla_prefill_mha"
+    _check(name, getattr(library(), name)(
         ctypes.byref(c), L, q.data_ptr(), T, H, w_ukv.data_ptr(), sm_scale, out.data_ptr(),
         _ptr(lse), ws.data_ptr(), ws.numel(), _stream(stream)))
     return out, lse

@@ -176,9 +176,11 @@ size_t mla_prefill_mha_workspace_size(int L, int H, int device) {
   return mla::mha_ws_layout(L, H, sms).total;
 }
 
-mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, int H,
-                             const void* w_ukv, float sm_scale, void* out, float* lse,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+mla_status_t run_mha(const mla_kv_t* kv, int L, const void* q, int T, int H, const void* w_ukv,
+                     float sm_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream, int precise) {
   g_last_launches = 0;
   mla_status_t st = check_kv(kv);
   if (st != MLA_OK) return st;
@@ -220,6 +222,7 @@ mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, in
   a.status = reinterpret_cast<unsigned*>(base + w.status);
   a.hdr = reinterpret_cast<mla::WsHeader*>(base);
   a.device = dev;
+  a.precise = precise;
   a.prof_start = g_prof_start;  // the profiling events bracket the attention kernel alone
   a.prof_stop = g_prof_stop;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -231,6 +234,20 @@ mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, in
     return MLA_ERR_CUDA;
   }
   return MLA_OK;
+}
+
+}  // namespace
+
+mla_status_t mla_prefill_mha(const mla_kv_t* kv, int L, const void* q, int T, int H,
+                             const void* w_ukv, float sm_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  return run_mha(kv, L, q, T, H, w_ukv, sm_scale, out, lse, workspace, workspace_bytes, stream, 1);
+}
+
+mla_status_t mla_prefill_mha_bf16(const mla_kv_t* kv, int L, const void* q, int T, int H,
+                                  const void* w_ukv, float sm_scale, void* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  return run_mha(kv, L, q, T, H, w_ukv, sm_scale, out, lse, workspace, workspace_bytes, stream, 0);
 }
 
 mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float sm_scale,

@@ -137,11 +137,16 @@ __host__ __device__ __forceinline__ int64_t range_of(int64_t x, int64_t total, i
   return ((x + 1) * n + total - 1) / total - 1;
 }
 
+// Up-projected 16-bit columns per head in kvup: bf16 form 128 key + 128 value columns;
+// precise form 128 key (hi) + 128 key (lo) + 128 value columns.
+inline __host__ __device__ int mha_up_width(bool precise) { return precise ? 384 : 256; }
+
 // MHA-form prefill workspace: header, status words (one per attention CTA, then one for the
 // dequantisation), the dequantised latent [L][512] bf16, the RoPE rows [L][64] bf16, the
-// up-projected keys and values [L][H][256] bf16 (per head 128 key dims, then 128 value
-// dims), and the partials of units split along the key axis: one slot per cluster of two
-// CTAs, each [2][128][128] float32 outputs and [2][128] float32 LSE.
+// up-projected keys and values [L][H][384] 16-bit (room for the precise form's hi, lo and
+// value columns; the bf16 form uses the first 256 columns' worth of each row), and the
+// partials of units split along the key axis: one slot per pair of CTAs, each
+// [2][128][128] float32 outputs and [2][128] float32 LSE.
 struct MhaWsLayout {
   size_t status, latent, rope, kvup, part_out, part_lse, total;
 };
@@ -155,7 +160,7 @@ inline MhaWsLayout mha_ws_layout(int64_t L, int H, int num_sms) {
   w.rope = off;
   off = align_up(off + (size_t)L * 64 * 2, 256);
   w.kvup = off;
-  off = align_up(off + (size_t)L * H * 256 * 2, 256);
+  off = align_up(off + (size_t)L * H * mha_up_width(true) * 2, 256);
   const size_t slots = (size_t)(num_sms / 2 + 1);
   w.part_out = off;
   off = align_up(off + slots * 2 * 128 * 128 * sizeof(float), 256);
@@ -185,6 +190,7 @@ struct MhaArgs {
   unsigned* status;   // [num attention CTAs + 1]
   WsHeader* hdr;
   int device;
+  int precise;        // 1: keys as bf16 hi + lo pairs, fp16 values and probabilities
   cudaEvent_t prof_start, prof_stop;  // recorded around the attention kernel when both set
 };
 
@@ -198,8 +204,8 @@ cudaError_t launch_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t
                                 const int64_t* slots, int64_t n, float inv, unsigned* status,
                                 int num_sms, cudaStream_t s);
 cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches);
-cudaError_t launch_mha_projection(const void* latent, const void* w, void* kvup, int L, int N,
-                                  float kv_scale, unsigned* status, cudaStream_t s);
+cudaError_t launch_mha_projection(const void* latent, const void* w, void* kvup, int L, int H,
+                                  float kv_scale, int precise, unsigned* status, cudaStream_t s);
 cudaError_t launch_top_k_renorm(const float* probs, float* out, int B, int V, const int32_t* top_k,
                                 int k_all, cudaStream_t s);
 

@@ -42,19 +42,34 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;                       // new positions per unit
-constexpr int kBN = 128;                       // keys per tile
-constexpr int kBox = 128 * 128;                // one 64-wide bf16 box of 128 rows (16 KB)
+constexpr int kBox = 128 * 128;                // one 64-wide 16-bit box of 128 rows (16 KB)
 constexpr int kQBytes = 3 * kBox;              // q: dims 0..63, 64..127, 128..191
-constexpr int kKBytes = 3 * kBox;              // keys: two up-projected boxes, then RoPE
-constexpr int kVBytes = 2 * kBox;              // values: dims 0..63, 64..127
 constexpr int kStages = 2;                     // key ring and value ring, two buffers each
 constexpr int kThreads = 384;                  // warp 0 TMA (q, keys), 1 MMA, 2 TMA (values), 4..11 softmax
-constexpr uint32_t kTmemCols = 512;            // S0, S1 [0,256); O0, O1 [256,512)
+constexpr uint32_t kTmemCols = 512;            // S0 at 0, S1 at 128; O0 at 256, O1 at 384
 constexpr uint32_t kColO = 256;
-constexpr int kOffK = kQBytes;
-constexpr int kOffV = kOffK + kStages * kKBytes;
-constexpr int kOffMisc = kOffV + kStages * kVBytes;
 constexpr uint64_t kWaitNs = 1000000000ull;    // every wait gives up after 1 s
+
+// The two forms of the attention (the host picks one per call).
+//   bf16 (PREC = false): keys [c W_UK ; r] x kv_scale and values in bf16, probabilities in
+//     bf16; 128-key tiles of three 64-wide key boxes.
+//   precise (PREC = true): keys as a bf16 pair hi + lo of c W_UK and the exact e4m3 RoPE
+//     values, all without kv_scale (it goes into the softmax scale), so the scores carry
+//     about 16 bits; values (x kv_scale) and probabilities in fp16; 96-key tiles of five
+//     key boxes (hi 0..63, hi 64..127, lo 0..63, lo 64..127, RoPE) so that the rings fit.
+template <bool PREC>
+struct MhaCfg {
+  static constexpr int kBN = PREC ? 96 : 128;    // keys per tile
+  static constexpr int kKBox = kBN * 128;        // one 64-wide 16-bit box of kBN keys
+  static constexpr int kKBytes = (PREC ? 5 : 3) * kKBox;
+  static constexpr int kVBytes = 2 * kKBox;      // values: dims 0..63, 64..127
+  static constexpr int kOffK = kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKBytes;
+  static constexpr int kOffMisc = kOffV + kStages * kVBytes;
+  static constexpr int kQKSteps = PREC ? 20 : 12;  // K = 16 MMAs of the scores
+  static constexpr int kValCol = PREC ? 256 : 128;  // first value column of a head in kvup
+  static constexpr uint32_t kPType = PREC ? 0 : 1;  // instruction type code: f16 : bf16
+};
 constexpr float kRescale = 8.f;                // log2 growth of a row maximum that forces a rescale
 
 struct Misc {
@@ -71,8 +86,11 @@ struct Misc {
   float red_sum[2][kBM];
 };
 
-constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory");
+template <bool PREC>
+constexpr int mha_smem_bytes() {
+  return MhaCfg<PREC>::kOffMisc + (int)sizeof(Misc) + 1024;  // + alignment slack
+}
+static_assert(mha_smem_bytes<false>() <= 232448 && mha_smem_bytes<true>() <= 232448, "shared memory");
 
 // 2^x on the SFU (the PTX instruction; inputs are <= 0 or -inf here)
 __device__ __forceinline__ float ex2(float x) {
@@ -83,7 +101,8 @@ __device__ __forceinline__ float ex2(float x) {
 
 struct MhaParams {
   int L, T, H;
-  float scale_log2;  // sm_scale * log2(e)
+  int bn;            // keys per tile (MhaCfg<PREC>::kBN)
+  float scale_log2;  // sm_scale * log2(e) (precise form: times kv_scale too)
   uint16_t* out;     // [T][H][128]
   float* lse;        // [T][H] or null
   unsigned* status;  // [gridDim.x]
@@ -119,7 +138,7 @@ struct Unit {
 __device__ __forceinline__ int num_qtiles(const MhaParams& p) { return (p.T + kBM - 1) / kBM; }
 __device__ __forceinline__ int num_pairs(const MhaParams& p) { return (num_qtiles(p) + 1) / 2; }
 
-__device__ __forceinline__ Unit unit_at(const MhaParams& p, int u, int rank) {
+__device__ __forceinline__ Unit unit_at(const MhaParams& p, int u, int rank, int bn) {
   const int nq = num_qtiles(p);
   const int qp = num_pairs(p) - 1 - u / p.H;
   const int hi = min(2 * qp + 1, nq - 1);         // the pair's later query tile
@@ -129,7 +148,7 @@ __device__ __forceinline__ Unit unit_at(const MhaParams& p, int u, int rank) {
   x.write = rank == 0 || hi != 2 * qp;
   const int last = min(hi * kBM + kBM, p.T) - 1;  // last new position of the later tile
   const int keys = p.L - p.T + last + 1;           // keys it sees
-  x.ntiles = (keys + kBN - 1) / kBN;
+  x.ntiles = (keys + bn - 1) / bn;
   return x;
 }
 
@@ -146,12 +165,12 @@ struct Split {
   int full_rounds, leftover, chunks_per_unit;  // chunks_per_unit < 2: leftovers run whole
 };
 
-__host__ __device__ __forceinline__ int mha_ntiles(int L, int T, int hi_tile) {
+__host__ __device__ __forceinline__ int mha_ntiles(int L, int T, int hi_tile, int bn) {
   const int last = (hi_tile * kBM + kBM < T ? hi_tile * kBM + kBM : T) - 1;
-  return (L - T + last + 1 + kBN - 1) / kBN;
+  return (L - T + last + 1 + bn - 1) / bn;
 }
 
-__host__ __device__ __forceinline__ Split split_of(int L, int T, int H, int clusters) {
+__host__ __device__ __forceinline__ Split split_of(int L, int T, int H, int clusters, int bn) {
   const int nq = (T + kBM - 1) / kBM, npairs = (nq + 1) / 2;
   const int U = npairs * H;
   Split sp;
@@ -160,7 +179,7 @@ __host__ __device__ __forceinline__ Split split_of(int L, int T, int H, int clus
   sp.chunks_per_unit = 1;
   if (sp.leftover > 0) {
     // the last unit (the smallest pair, 2 * 0 and 1) bounds how finely a unit can be cut
-    const int fewest = mha_ntiles(L, T, nq > 1 ? 1 : 0);
+    const int fewest = mha_ntiles(L, T, nq > 1 ? 1 : 0, bn);
     const int c = clusters / sp.leftover;
     sp.chunks_per_unit = c < fewest ? c : fewest;
   }
@@ -175,12 +194,12 @@ struct Work {
 };
 
 __device__ __forceinline__ Work work_at(const MhaParams& p, const Split& sp, int i, int c, int NC,
-                                        int rank) {
+                                        int rank, int bn) {
   Work w;
   w.valid = false;
   w.slot = -1;
   if (i < sp.full_rounds) {
-    w.x = unit_at(p, unit_of(i, c, NC), rank);
+    w.x = unit_at(p, unit_of(i, c, NC), rank, bn);
     w.j0 = 0;
     w.j1 = w.x.ntiles;
     w.valid = true;
@@ -190,7 +209,7 @@ __device__ __forceinline__ Work work_at(const MhaParams& p, const Split& sp, int
   const int base = sp.full_rounds * NC;
   if (sp.chunks_per_unit < 2) {
     if (c >= sp.leftover) return w;
-    w.x = unit_at(p, base + c, rank);
+    w.x = unit_at(p, base + c, rank, bn);
     w.j0 = 0;
     w.j1 = w.x.ntiles;
     w.valid = true;
@@ -198,7 +217,7 @@ __device__ __forceinline__ Work work_at(const MhaParams& p, const Split& sp, int
   }
   if (c >= sp.leftover * sp.chunks_per_unit) return w;
   const int lu = c % sp.leftover, kc = c / sp.leftover;
-  w.x = unit_at(p, base + lu, rank);
+  w.x = unit_at(p, base + lu, rank, bn);
   w.j0 = kc * w.x.ntiles / sp.chunks_per_unit;
   w.j1 = (kc + 1) * w.x.ntiles / sp.chunks_per_unit;
   w.slot = c;
@@ -206,6 +225,7 @@ __device__ __forceinline__ Work work_at(const MhaParams& p, const Split& sp, int
   return w;
 }
 
+template <bool PREC>
 __global__ void __launch_bounds__(kThreads, 1)
     mha_attn_kernel(const MhaParams p, const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kv,
@@ -213,11 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Misc* ms = reinterpret_cast<Misc*>(smem + kOffMisc);
+  using C = MhaCfg<PREC>;
+  constexpr int kBN = C::kBN;
+  Misc* ms = reinterpret_cast<Misc*>(smem + C::kOffMisc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x / 2, c = blockIdx.x / 2;  // pairs of neighbouring CTAs
   const int rank = (int)(blockIdx.x & 1);
-  const Split sp = split_of(p.L, p.T, p.H, G);
+  const Split sp = split_of(p.L, p.T, p.H, G, kBN);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int g = 0, k = 0;
       for (int r = 0;; ++r) {
-        const Work wk = work_at(p, sp, r, c, G, rank);
+        const Work wk = work_at(p, sp, r, c, G, rank, kBN);
         if (!wk.valid || ms->abort) break;
         const Unit& x = wk.x;
         if (k > 0 && !wait_or_abort(&ms->q_free, (k - 1) & 1, ms)) break;
@@ -263,12 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = wk.j0; j < wk.j1; ++j, ++g) {
           const int s = g & 1;
           if (g >= 2 && !(ok = wait_or_abort(&ms->k_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
-          uint8_t* kb = smem + kOffK + s * kKBytes;
-          mbar_arrive_expect_tx(&ms->k_full[s], kKBytes);
+          uint8_t* kb = smem + C::kOffK + s * C::kKBytes;
+          mbar_arrive_expect_tx(&ms->k_full[s], C::kKBytes);
           const int n0 = j * kBN;
-          tma_load_3d(kb, &map_kv, 0, x.h, n0, &ms->k_full[s]);
-          tma_load_3d(kb + kBox, &map_kv, 64, x.h, n0, &ms->k_full[s]);
-          tma_load_2d(kb + 2 * kBox, &map_rope, 0, n0, &ms->k_full[s]);
+          // the up-projected boxes (bf16: two; precise: hi, hi, lo, lo), then RoPE
+          constexpr int kUp = PREC ? 4 : 2;
+#pragma unroll
+          for (int bx = 0; bx < kUp; ++bx)
+            tma_load_3d(kb + bx * C::kKBox, &map_kv, 64 * bx, x.h, n0, &ms->k_full[s]);
+          tma_load_2d(kb + kUp * C::kKBox, &map_rope, 0, n0, &ms->k_full[s]);
         }
         if (!ok) break;
         ++k;
@@ -280,39 +305,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const Work wk = work_at(p, sp, r, c, G, rank);
+        const Work wk = work_at(p, sp, r, c, G, rank, kBN);
         if (!wk.valid || ms->abort) break;
         const Unit& x = wk.x;
         for (int j = wk.j0; j < wk.j1; ++j, ++g) {
           const int s = g & 1;
           if (g >= 2 && !(ok = wait_or_abort(&ms->v_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
-          uint8_t* vb = smem + kOffV + s * kVBytes;
-          mbar_arrive_expect_tx(&ms->v_full[s], kVBytes);
-          tma_load_3d(vb, &map_kv, 128, x.h, j * kBN, &ms->v_full[s]);
-          tma_load_3d(vb + kBox, &map_kv, 192, x.h, j * kBN, &ms->v_full[s]);
+          uint8_t* vb = smem + C::kOffV + s * C::kVBytes;
+          mbar_arrive_expect_tx(&ms->v_full[s], C::kVBytes);
+          tma_load_3d(vb, &map_kv, C::kValCol, x.h, j * kBN, &ms->v_full[s]);
+          tma_load_3d(vb + C::kKBox, &map_kv, C::kValCol + 64, x.h, j * kBN, &ms->v_full[s]);
         }
       }
     }
   } else if (warp == 1) {
     // ---- MMA issuer ----
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = instr_desc(1, 1, 0, 0, 128, 128);  // bf16, both K-major
-      constexpr uint32_t idesc_pv = instr_desc(1, 1, 0, 1, 128, 128);  // P from TMEM, V MN-major
+      constexpr uint32_t idesc_qk = instr_desc(1, 1, 0, 0, 128, kBN);  // bf16, both K-major
+      // P from TMEM, V MN-major from shared memory (both bf16, or both f16 when precise)
+      constexpr uint32_t idesc_pv = instr_desc(C::kPType, C::kPType, 0, 1, 128, 128);
       const uint32_t q_addr = smem_addr(smem);
-      const uint32_t k_base = smem_addr(smem + kOffK);
-      const uint32_t v_base = smem_addr(smem + kOffV);
+      const uint32_t k_base = smem_addr(smem + C::kOffK);
+      const uint32_t v_base = smem_addr(smem + C::kOffV);
       // values MMA of tile gx: P from the score buffer of parity gx & 1 into that parity's
       // O accumulator; `first`: the first tile of this parity in the unit
       auto pv = [&](int gx, bool first) -> bool {
         if (!wait_or_abort(&ms->p_full[gx & 1], (gx >> 1) & 1, ms)) return false;
         if (!wait_or_abort(&ms->v_full[gx & 1], (gx >> 1) & 1, ms)) return false;
         tc_fence_after();
-        const uint32_t v_addr = v_base + (gx & 1) * kVBytes;
+        const uint32_t v_addr = v_base + (gx & 1) * C::kVBytes;
         const uint32_t pcol = tmem + (gx & 1) * 128;
         const uint32_t ocol = tmem + kColO + (gx & 1) * 128;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t b = smem_desc(v_addr + ks * 2048, kBox, 1024, Swizzle::k128B);
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t b = smem_desc(v_addr + ks * 2048, C::kKBox, 1024, Swizzle::k128B);
           mma_f16_tmem_a(ocol, pcol + ks * 8, b, idesc_pv, (first && ks == 0) ? 0u : 1u);
         }
         mma_commit(&ms->v_empty[gx & 1]);
@@ -322,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, k = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const Work wk = work_at(p, sp, r, c, G, rank);
+        const Work wk = work_at(p, sp, r, c, G, rank, kBN);
         if (!wk.valid || ms->abort) break;
         const int n = wk.j1 - wk.j0;  // tiles of this work item
         if (!(ok = wait_or_abort(&ms->q_full, k & 1, ms))) break;
@@ -330,12 +356,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g & 1;
           if (!(ok = wait_or_abort(&ms->k_full[s], (g >> 1) & 1, ms))) break;
           tc_fence_after();
-          const uint32_t k_addr = k_base + s * kKBytes;
+          const uint32_t k_addr = k_base + s * C::kKBytes;
 #pragma unroll
-          for (int kk = 0; kk < 12; ++kk) {
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            const uint64_t a = smem_desc(q_addr + off, 16, 1024, Swizzle::k128B);
-            const uint64_t b = smem_desc(k_addr + off, 16, 1024, Swizzle::k128B);
+          for (int kk = 0; kk < C::kQKSteps; ++kk) {
+            // k-step kk: query box qb against key box kb (precise: dims 0..127 against the
+            // hi boxes, again against the lo boxes, then the RoPE dims)
+            const int qb = PREC ? (kk < 16 ? (kk & 7) >> 2 : 2) : kk >> 2;
+            const int kb = PREC ? (kk < 16 ? kk >> 2 : 4) : kk >> 2;
+            const uint32_t in_box = (kk & 3) * 32;
+            const uint64_t a = smem_desc(q_addr + qb * kBox + in_box, 16, 1024, Swizzle::k128B);
+            const uint64_t b = smem_desc(k_addr + kb * C::kKBox + in_box, 16, 1024, Swizzle::k128B);
             mma_f16(tmem + s * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&ms->s_full[s]);
@@ -364,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const Work wk = work_at(p, sp, r, c, G, rank);
+      const Work wk = work_at(p, sp, r, c, G, rank, kBN);
       if (!wk.valid || ms->abort) break;
       const Unit& x = wk.x;
       const int t = x.q0 + row;          // new position of this thread's row
@@ -384,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pass 1: the row maximum (log2 units)
         float mt = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kBN / 32; ++q) {
           float a[16], b[16];
           tmem_ld16(s_col + 32 * q, a);
           tmem_ld16(s_col + 32 * q + 16, b);
@@ -414,12 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m_run = mt;
         }
-        // pass 2: probabilities, packed two bf16 per column over the first 64 score columns
-        // (column 16q + i holds keys 32q + 2i, 32q + 2i + 1; chunk q's packed columns only
-        // overlap score columns already read)
+        // pass 2: probabilities, packed two 16-bit values per column over the first kBN / 2
+        // score columns (column 16q + i holds keys 32q + 2i, 32q + 2i + 1; chunk q's packed
+        // columns only overlap score columns already read)
         float sum = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kBN / 32; ++q) {
           float a[16], b[16];
           tmem_ld16(s_col + 32 * q, a);
           tmem_ld16(s_col + 32 * q + 16, b);
@@ -438,10 +468,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(y0), p3 = ex2(y1);
             sum += (p0 + p1) + (p2 + p3);
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
-            pk[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h0));
-            pk[8 + e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
+            if constexpr (PREC) {
+              const __half2 h0 = __floats2half2_rn(p0, p1), h1 = __floats2half2_rn(p2, p3);
+              pk[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h0));
+              pk[8 + e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
+            } else {
+              const __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
+              const __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
+              pk[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h0));
+              pk[8 + e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
+            }
           }
           tmem_st16(s_col + 16 * q, pk);
         }
@@ -536,7 +572,7 @@ __global__ void __launch_bounds__(256) mha_chunk_merge_kernel(const MhaParams p,
   const int lane = threadIdx.x & 31;
   if (wid >= sp.leftover * 2 * kBM) return;
   const int lu = wid / (2 * kBM), rank = (wid / kBM) & 1, row = wid % kBM;
-  const Unit x = unit_at(p, sp.full_rounds * NC + lu, rank);
+  const Unit x = unit_at(p, sp.full_rounds * NC + lu, rank, p.bn);
   const int t = x.q0 + row;
   if (!x.write || t >= p.T) return;
   const int nch = sp.chunks_per_unit;
@@ -566,10 +602,11 @@ __global__ void __launch_bounds__(256) mha_chunk_merge_kernel(const MhaParams p,
 }
 
 // Cached rows -> latent [L][512] bf16 (the e4m3 values; exact) and RoPE rows [L][64] bf16
-// (e4m3 value x kv_scale, one rounding). One thread per 8 codes of a row.
+// (e4m3 value x rope_scale: kv_scale, one rounding, for the bf16 form; 1, exact, for the
+// precise one). One thread per 8 codes of a row.
 __global__ void mha_dequant_kernel(const uint8_t* __restrict__ pool, int64_t num_pages,
                                    int page_size, const int32_t* __restrict__ page_table, int L,
-                                   float kv_scale, __nv_bfloat16* __restrict__ latent,
+                                   float rope_scale, __nv_bfloat16* __restrict__ latent,
                                    __nv_bfloat16* __restrict__ rope, unsigned* status) {
   const int64_t items = (int64_t)L * (kD / 8);
   for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
@@ -605,7 +642,7 @@ __global__ void mha_dequant_kernel(const uint8_t* __restrict__ pool, int64_t num
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i] * kv_scale, f[2 * i + 1] * kv_scale);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i] * rope_scale, f[2 * i + 1] * rope_scale);
         o[i] = *reinterpret_cast<const uint32_t*>(&b);
       }
       *reinterpret_cast<uint4*>(rope + (int64_t)n * 64 + (c8 - kDV / 8) * 8) =
@@ -638,26 +675,11 @@ static EncodeFn tensor_map_encoder() {
   return fn;
 }
 
-cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches) {
-  const int pairs = (((a.T + kBM - 1) / kBM) + 1) / 2 * a.H;
-  const int grid = 2 * std::min(num_sms / 2, pairs);  // pairs of CTAs
-  // 1. dequantise (its status word follows the attention CTAs' words and is cleared first)
-  unsigned* dq_status = a.status + grid;
-  cudaError_t e = cudaMemsetAsync(dq_status, 0, sizeof(unsigned), s);
-  if (e != cudaSuccess) return e;
-  const int64_t items = (int64_t)a.L * (kD / 8);
-  const int grid1 = (int)std::min<int64_t>((items + 255) / 256, (int64_t)num_sms * 8);
-  mha_dequant_kernel<<<grid1, 256, 0, s>>>(a.pool, a.num_pages, a.page_size, a.page_table, a.L,
-                                           a.kv_scale, reinterpret_cast<__nv_bfloat16*>(a.latent),
-                                           reinterpret_cast<__nv_bfloat16*>(a.rope), dq_status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ++*launches;
-  // 2. up-projection: kvup [L][H*256] = kv_scale * latent [L][512] @ w_ukv [512][H*256]
-  e = launch_mha_projection(a.latent, a.w_ukv, a.kvup, a.L, a.H * 256, a.kv_scale, dq_status, s);
-  if (e != cudaSuccess) return e;
-  ++*launches;
-  // 3. attention
+// The attention launch of one form: tensor maps over q, kvup and the RoPE rows, the
+// attention kernel, and the merge of key-split units when the last round was cut.
+template <bool PREC>
+static cudaError_t launch_mha_attn(const MhaArgs& a, int grid, cudaStream_t s, int* launches) {
+  using C = MhaCfg<PREC>;
   const EncodeFn encode = tensor_map_encoder();
   if (!encode) return cudaErrorInvalidValue;
   CUtensorMap mq, mkv, mr;
@@ -672,9 +694,12 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
       return cudaErrorInvalidValue;
   }
   {
-    cuuint64_t dims[3] = {256, (cuuint64_t)a.H, (cuuint64_t)a.L};
-    cuuint64_t strides[2] = {256 * 2, (cuuint64_t)a.H * 256 * 2};
-    cuuint32_t box[3] = {64, 1, 128};
+    // kvup [L][H][width] 16-bit (precise: hi, lo, then fp16 values; the map moves bytes
+    // only, so one 16-bit element type serves all of them)
+    const cuuint64_t width = mha_up_width(PREC);
+    cuuint64_t dims[3] = {width, (cuuint64_t)a.H, (cuuint64_t)a.L};
+    cuuint64_t strides[2] = {width * 2, (cuuint64_t)a.H * width * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)C::kBN};
     if (encode(&mkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kvup, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -683,7 +708,7 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
   {
     cuuint64_t dims[2] = {64, (cuuint64_t)a.L};
     cuuint64_t strides[1] = {64 * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, (cuuint32_t)C::kBN};
     if (encode(&mr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.rope, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -693,27 +718,25 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
   p.L = a.L;
   p.T = a.T;
   p.H = a.H;
-  p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.bn = C::kBN;
+  p.scale_log2 = a.sm_scale * (PREC ? a.kv_scale : 1.f) * 1.4426950408889634f;
   p.out = a.out;
   p.lse = a.lse;
   p.status = a.status;
   p.hdr = a.hdr;
   p.part_out = static_cast<float*>(a.part_out);
   p.part_lse = static_cast<float*>(a.part_lse);
-  e = cudaFuncSetAttribute(mha_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  constexpr int smem = mha_smem_bytes<PREC>();
+  cudaError_t e = cudaFuncSetAttribute(mha_attn_kernel<PREC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const bool prof = a.prof_start && a.prof_stop;
   if (prof) cudaEventRecord(a.prof_start, s);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  e = cudaLaunchKernelEx(&cfg, mha_attn_kernel, p, mq, mkv, mr);
+  mha_attn_kernel<PREC><<<grid, kThreads, smem, s>>>(p, mq, mkv, mr);
+  e = cudaGetLastError();
   if (e == cudaSuccess) ++*launches;
   if (prof) cudaEventRecord(a.prof_stop, s);
   // the split units' partials (only when the last round was cut into chunks)
-  const Split sp = split_of(a.L, a.T, a.H, grid / 2);
+  const Split sp = split_of(a.L, a.T, a.H, grid / 2, C::kBN);
   if (e == cudaSuccess && sp.leftover > 0 && sp.chunks_per_unit >= 2) {
     const int warps = sp.leftover * 2 * kBM;
     mha_chunk_merge_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p, sp, grid / 2);
@@ -721,6 +744,32 @@ cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, in
     if (e == cudaSuccess) ++*launches;
   }
   return e;
+}
+
+cudaError_t launch_mha_prefill(const MhaArgs& a, int num_sms, cudaStream_t s, int* launches) {
+  const int pairs = (((a.T + kBM - 1) / kBM) + 1) / 2 * a.H;
+  const int grid = 2 * std::min(num_sms / 2, pairs);  // pairs of CTAs
+  // 1. dequantise (its status word follows the attention CTAs' words and is cleared first);
+  //    the precise form keeps the RoPE values exact and applies kv_scale in the softmax
+  unsigned* dq_status = a.status + grid;
+  cudaError_t e = cudaMemsetAsync(dq_status, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  const int64_t items = (int64_t)a.L * (kD / 8);
+  const int grid1 = (int)std::min<int64_t>((items + 255) / 256, (int64_t)num_sms * 8);
+  mha_dequant_kernel<<<grid1, 256, 0, s>>>(a.pool, a.num_pages, a.page_size, a.page_table, a.L,
+                                           a.precise ? 1.f : a.kv_scale,
+                                           reinterpret_cast<__nv_bfloat16*>(a.latent),
+                                           reinterpret_cast<__nv_bfloat16*>(a.rope), dq_status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  // 2. up-projection: latent [L][512] @ w_ukv [512][H*256] into kvup [L][H][width]
+  e = launch_mha_projection(a.latent, a.w_ukv, a.kvup, a.L, a.H, a.kv_scale, a.precise, dq_status, s);
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  // 3. attention
+  return a.precise ? launch_mha_attn<true>(a, grid, s, launches)
+                   : launch_mha_attn<false>(a, grid, s, launches);
 }
 
 }  // namespace mla

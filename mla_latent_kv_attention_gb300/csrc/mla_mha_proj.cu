@@ -1,19 +1,25 @@
 // mla_mha_proj.cu -- the up-projection of the MHA-form prefill, on tcgen05.
 //
 // Keys and values of every head come from the one shared latent ("MI355X Kimi K2.5 vLLM
-// AITER 7x speedup", section "PR #35850 修复了什么"): for cached row n and output column c,
-//     kvup[n][c] = kv_scale * sum_k latent[n][k] * w_ukv[k][c]
-// with latent [L][512] bf16 (the rows' e4m3 values, exact), w_ukv [512][H*256] bf16 (per
-// head 128 key columns, then 128 value columns) and kvup [L][H*256] bf16.
+// AITER 7x speedup", section "PR #35850 修复了什么"): for cached row n and column c of head h,
+//     acc[n][h][c] = sum_k latent[n][k] * w_ukv[k][h][c]
+// with latent [L][512] bf16 (the rows' e4m3 values, exact) and w_ukv [512][H][256] bf16 (per
+// head 128 key columns, then 128 value columns). kvup [L][H][width] receives
+//   bf16 form (width 256): kv_scale * acc rounded to bf16, keys and values alike;
+//   precise form (width 384): for the key columns acc itself as a bf16 pair, hi = bf16(acc)
+//     in columns 0..127 and lo = bf16(acc - hi) in 128..255 (about 16 bits; kv_scale is
+//     applied with the softmax scale), for the value columns kv_scale * acc rounded to fp16
+//     in 256..383.
 //
 // One CTA per 128 x 256 output tile. TMA brings 64-wide k-blocks of both operands into a
 // two-stage ring (the latent tile K-major, the weight tile MN-major, both 128-byte
 // swizzled); one thread issues M = 128, N = 256, K = 16 bf16 MMAs into a 256-column TMEM
-// accumulator; the four warps read it back (one row per thread), scale by kv_scale, round
-// to bf16 and store. Two CTAs fit an SM, so one tile's epilogue overlaps another's loads.
+// accumulator; the four warps read it back (one row per thread), round as above and store.
+// Two CTAs fit an SM, so one tile's epilogue overlaps another's loads.
 // Every wait is bounded; a wait that gives up reports MLA_ERR_TIMEOUT in the status word.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,7 +54,7 @@ static_assert(2 * kPSmem <= 232448, "two CTAs per SM");
 
 __global__ void __launch_bounds__(128, 2)
     mha_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                    int L, int N, float scale, uint16_t* __restrict__ out, unsigned* status) {
+                    int L, int N, float scale, int precise, uint16_t* __restrict__ out, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -122,22 +128,42 @@ __global__ void __launch_bounds__(128, 2)
   const int row = m0 + warp * 32 + lane;
   if (ok) {
     const uint32_t base = tmem + ((uint32_t)(warp * 32) << 16);
-    uint16_t* dst = out + (int64_t)row * N + n0;
+    // a tile is one head's 256 columns (n0 = 256 h)
+    const int width = precise ? 384 : 256, H = N / kPN;
+    uint16_t* dst = out + ((int64_t)row * H + n0 / kPN) * width;
 #pragma unroll 1
     for (int c = 0; c < kPN; c += 16) {
       float v[16];
       tmem_ld16(base + c, v);
       tmem_wait_ld();
-      uint32_t w[8];
+      uint32_t w[8], lo[8];
+      const bool key = c < kPN / 2;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e] * scale, v[2 * e + 1] * scale);
-        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+        if (!precise) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e] * scale, v[2 * e + 1] * scale);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h);
+        } else if (key) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+          const float2 hf = __bfloat1622float2(h);
+          const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h);
+          lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+        } else {
+          const __half2 h = __floats2half2_rn(v[2 * e] * scale, v[2 * e + 1] * scale);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
       }
       if (row < L) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+        // bf16 form: column c; precise form: keys hi at c and lo at 128 + c, values at 128 + c
+        uint4* d4 = reinterpret_cast<uint4*>(dst + ((precise && !key) ? c + 128 : c));
         d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (precise && key) {
+          uint4* l4 = reinterpret_cast<uint4*>(dst + 128 + c);
+          l4[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          l4[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
       }
     }
   } else if (threadIdx.x == 0 && status) {
@@ -179,12 +205,13 @@ EncodeFn proj_encoder() {
 
 }  // namespace
 
-// kvup [L][N] = kv_scale * latent [L][512] @ w [512][N]; N a multiple of 256, pointers
-// 16-byte aligned. One launch.
-cudaError_t launch_mha_projection(const void* latent, const void* w, void* kvup, int L, int N,
-                                  float kv_scale, unsigned* status, cudaStream_t s) {
+// latent [L][512] @ w [512][H][256] into kvup [L][H][mha_up_width(precise)] (see the top of
+// this file); pointers 16-byte aligned. One launch.
+cudaError_t launch_mha_projection(const void* latent, const void* w, void* kvup, int L, int H,
+                                  float kv_scale, int precise, unsigned* status, cudaStream_t s) {
   if (L <= 0) return cudaSuccess;
-  if (N <= 0 || N % kPN != 0) return cudaErrorInvalidValue;
+  const int N = H * kPN;
+  if (H <= 0) return cudaErrorInvalidValue;
   const EncodeFn encode = proj_encoder();
   if (!encode) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
@@ -210,7 +237,7 @@ cudaError_t launch_mha_projection(const void* latent, const void* w, void* kvup,
   cudaError_t e = cudaFuncSetAttribute(mha_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = (int64_t)((L + kPM - 1) / kPM) * (N / kPN);
-  mha_proj_kernel<<<(unsigned)tiles, 128, kPSmem, s>>>(ma, mb, L, N, kv_scale,
+  mha_proj_kernel<<<(unsigned)tiles, 128, kPSmem, s>>>(ma, mb, L, N, kv_scale, precise,
                                                         static_cast<uint16_t*>(kvup), status);
   return cudaGetLastError();
 }

@@ -1,6 +1,8 @@
 """MHA-form causal prefill (latent up-projected per head, then dense causal attention)
 against the float64 oracle, through the C ABI. Small cases on every row; the full chunk
-(8,192 new positions on a 32,768 prefix, 12 heads) on sampled rows."""
+(8,192 new positions on a 32,768 prefix, 12 heads) on sampled rows. The default form is held
+to the absorbed path's relative L2 and LSE bounds; the bf16 form (mla_prefill_mha_bf16) to
+its own, looser ones (tests/parity.py)."""
 import numpy as np
 import pytest
 import torch
@@ -8,18 +10,25 @@ import torch
 import mla_latent_kv_attention_gb300 as mla
 import oracle
 from mla_latent_kv_attention_gb300 import workloads as W
-from tests.parity import MHA_LSE_REL, MHA_MAX_ABS_ROW, MHA_REL_L2, compare
+from tests.parity import (LSE_REL, MHA_BF16_LSE_REL, MHA_BF16_REL_L2, MHA_MAX_ABS_ROW, REL_L2,
+                          compare)
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 
 
-def run(m):
+def run(m, bf16=False):
     kv = mla.KVCache.from_inputs(m.cache, DEV)
-    out, lse = mla.mla_prefill_mha(kv, m.q.to(DEV), m.w_ukv.to(DEV), m.cache.sm_scale)
+    out, lse = mla.mla_prefill_mha(kv, m.q.to(DEV), m.w_ukv.to(DEV), m.cache.sm_scale, bf16=bf16)
     torch.cuda.synchronize()
     return out, lse
+
+
+def check(got, gl, ref_out, ref_lse, what, bf16=False):
+    return compare(got, gl, ref_out, ref_lse, what,
+                   rel_l2=MHA_BF16_REL_L2 if bf16 else REL_L2,
+                   lse_rel=MHA_BF16_LSE_REL if bf16 else LSE_REL, max_abs_row=MHA_MAX_ABS_ROW)
 
 
 # (1280, 1000, 16): 80 pairs of query tiles for 76 clusters, so the four pairs of the last
@@ -30,8 +39,15 @@ def test_mha_prefill_small(T, prefix, H):
     m = W.mha_prefill_inputs(T, prefix, H=H, seed=T + prefix + H)
     out, lse = run(m)
     ref_out, ref_lse = oracle.mha_prefill_rows(m.cache, m.q, m.w_ukv)
-    compare(out, lse, ref_out, ref_lse, f"mha T={T} prefix={prefix} H={H}", rel_l2=MHA_REL_L2, lse_rel=MHA_LSE_REL,
-            max_abs_row=MHA_MAX_ABS_ROW)
+    check(out, lse, ref_out, ref_lse, f"mha T={T} prefix={prefix} H={H}")
+
+
+@pytest.mark.parametrize("T,prefix,H", [(128, 0, 1), (384, 1000, 12), (1280, 1000, 16)])
+def test_mha_prefill_bf16_form(T, prefix, H):
+    m = W.mha_prefill_inputs(T, prefix, H=H, seed=T + prefix + H)
+    out, lse = run(m, bf16=True)
+    ref_out, ref_lse = oracle.mha_prefill_rows(m.cache, m.q, m.w_ukv)
+    check(out, lse, ref_out, ref_lse, f"mha bf16 T={T} prefix={prefix} H={H}", bf16=True)
 
 
 def test_mha_prefill_matches_absorbed_kernel_path():
@@ -59,12 +75,11 @@ def test_mha_prefill_matches_absorbed_kernel_path():
     out_a, lse_a = mla.mla_prefill(kv, qa, m.cache.sm_scale)
     torch.cuda.synchronize()
     ref_out, ref_lse = oracle.mha_prefill_rows(m.cache, m.q, w)
-    compare(out, lse, ref_out, ref_lse, "mha selection", rel_l2=MHA_REL_L2, lse_rel=MHA_LSE_REL,
-            max_abs_row=MHA_MAX_ABS_ROW)
+    check(out, lse, ref_out, ref_lse, "mha selection")
     oa = out_a.float().cpu().numpy()
     picked = np.stack([oa[:, h][:, sel[h]] for h in range(H)], 1)
     got = out.float().cpu().numpy()
-    assert np.linalg.norm(got - picked) / np.linalg.norm(picked) < MHA_REL_L2
+    assert np.linalg.norm(got - picked) / np.linalg.norm(picked) < REL_L2
 
 
 def test_mha_prefill_full_chunk_sampled_rows():
@@ -76,8 +91,7 @@ def test_mha_prefill_full_chunk_sampled_rows():
     ref_out, ref_lse = oracle.mha_prefill_rows(m.cache, m.q, m.w_ukv, rows)
     got = out[rows[:, 0], rows[:, 1]]
     gl = lse[rows[:, 0], rows[:, 1]]
-    compare(got, gl, ref_out, ref_lse, "mha full chunk", rel_l2=MHA_REL_L2, lse_rel=MHA_LSE_REL,
-            max_abs_row=MHA_MAX_ABS_ROW)
+    check(got, gl, ref_out, ref_lse, "mha full chunk")
 
 
 def test_mha_prefill_reports_no_error():
@@ -96,8 +110,7 @@ def test_mha_prefill_larger_pages(page_size):
     m = W.mha_prefill_inputs(300, 700, H=4, seed=page_size, page_size=page_size)
     out, lse = run(m)
     ref_out, ref_lse = oracle.mha_prefill_rows(m.cache, m.q, m.w_ukv)
-    compare(out, lse, ref_out, ref_lse, f"mha pages of {page_size}", rel_l2=MHA_REL_L2,
-            lse_rel=MHA_LSE_REL, max_abs_row=MHA_MAX_ABS_ROW)
+    check(out, lse, ref_out, ref_lse, f"mha pages of {page_size}")
 
 
 def test_mha_prefill_reports_a_page_outside_the_pool():
