@@ -26,11 +26,12 @@ def main(argv=None) -> int:
     ap.add_argument("--iters", type=int, default=5)
     ap.add_argument("--heads", type=int, default=12, help="long_history_decode only")
     ap.add_argument("--T", type=int, default=8192, help="causal_prefill and mha_prefill only")
+    ap.add_argument("--bf16", action="store_true", help="mha_prefill only: the all-bf16 form")
     args = ap.parse_args(argv)
     if args.workload == "cache_append":
         return _cache_append(args.iters)
     if args.workload == "mha_prefill":
-        return _mha_prefill(args.T, args.iters)
+        return _mha_prefill(args.T, args.iters, args.bf16)
     if args.workload == "top_k_renorm":
         return _top_k_renorm(args.iters)
     if args.workload == "long_history_decode":
@@ -75,8 +76,9 @@ def _cache_append(iters: int) -> int:
     return 0 if st == 0 else 1
 
 
-def _mha_prefill(T: int, iters: int) -> int:
-    """The causal prefill chunk (T new positions on a 32,768 prefix, 12 heads) in the MHA form."""
+def _mha_prefill(T: int, iters: int, bf16: bool = False) -> int:
+    """The causal prefill chunk (T new positions on a 32,768 prefix, 12 heads) in the MHA form
+    (the default form, or the all-bf16 one)."""
     m = W.mha_prefill(T=T)
     kv = mla.KVCache.from_inputs(m.cache, "cuda")
     q = m.q.cuda()
@@ -85,7 +87,7 @@ def _mha_prefill(T: int, iters: int) -> int:
     ws = torch.zeros(mla.library().mla_prefill_mha_workspace_size(L, m.H, 0), dtype=torch.uint8,
                      device="cuda")
     for _ in range(iters):
-        mla.mla_prefill_mha(kv, q, w, m.cache.sm_scale, L=L, ws=ws)
+        mla.mla_prefill_mha(kv, q, w, m.cache.sm_scale, L=L, ws=ws, bf16=bf16)
     torch.cuda.synchronize()
     status = mla.mla_read_status(ws)
     print(f"mha_prefill: {iters} calls, status {mla.STATUS.get(status, status)}")
