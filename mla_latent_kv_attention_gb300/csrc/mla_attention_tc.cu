@@ -56,6 +56,18 @@ constexpr int kTileKeys = 128;
 constexpr int kStages = 2;
 constexpr int kChunkBytes = 16384;                     // 128 keys x 128 bytes, SW128
 constexpr int kStageBytes = 4 * kChunkBytes + 2 * 4096;  // 73,728 bytes loaded per tile
+// A stage is filled and freed in two halves: latent chunks 0-1, then chunks 2-3 with the
+// RoPE tail. The values MMA frees the first half as soon as its own MMAs complete, so the
+// next tile's first half loads while the second is still being read. (Every
+// tcgen05.commit costs the issuing thread time: measured, five parts ran slower than one,
+// two fastest.)
+constexpr int kParts = 2;
+__host__ __device__ constexpr int part_of_chunk(int c) { return c / 2; }
+constexpr int kTailPart = 1;
+__host__ __device__ constexpr int part_bytes(int part) {
+  return part == 0 ? 2 * kChunkBytes : 2 * kChunkBytes + 2 * 4096;
+}
+static_assert(part_bytes(0) + part_bytes(1) == kStageBytes, "the halves make up the stage");
 constexpr int kMaxThreads = 512;  // producer, 2 MMA issuers, query stager, 2-3 softmax warpgroups
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s
@@ -127,11 +139,11 @@ struct Misc {
   alignas(16) int grow[2][12];       // per tile parity and warp: some row's max moves
   alignas(16) int row_j[48];         // new-position index j of each row (very negative for padding)
   alignas(16) int row_off[48];       // j * H + h: the row's index among its sequence's rows
-  alignas(8) uint64_t kv_full[kStages], kv_empty[kStages];
+  alignas(8) uint64_t kv_full[kStages][kParts];  // part landed (TMA transaction bytes)
+  uint64_t kv_free[kStages][kParts];             // part no longer read by any MMA
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2];   // P of tile g is written: p_full[g % 2] (the softmax may run a tile
                         // ahead of the value MMAs when P lives in the stage)
-  uint64_t pv_done[2];  // PV of tile g completes pv_done[g % 2]
   uint64_t q_full[2];   // query operand buffer holds its unit's terms
   uint64_t q_empty[2];  // the unit that used the buffer has finished its scores
   uint64_t q0_done;     // the first unit's query rows are staged (by warps 2.. together)
@@ -454,10 +466,11 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   if (trace && threadIdx.x == 0) trace[kTrEntry] = globaltimer_ns();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ms->kv_full[s], 1);
-      mbar_init(&ms->kv_empty[s], 1);
-    }
+    for (int s = 0; s < kStages; ++s)
+      for (int c = 0; c < kParts; ++c) {
+        mbar_init(&ms->kv_full[s][c], 1);
+        mbar_init(&ms->kv_free[s][c], 1);
+      }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->s_full[s], 1);
       mbar_init(&ms->s_empty[s], 128 * C::kNWG);
@@ -465,8 +478,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     for (int w = 0; w < C::kNWG; ++w) mbar_init(&ms->wg_bar[w], 128);
     mbar_init(&ms->p_full[0], 128 * C::kNWG);
     mbar_init(&ms->p_full[1], 128 * C::kNWG);
-    mbar_init(&ms->pv_done[0], 1);
-    mbar_init(&ms->pv_done[1], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->q_full[s], 1);
       mbar_init(&ms->q_empty[s], 1);
@@ -657,41 +668,58 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
           const int s = fill % kStages;
           const uint32_t n = fill / kStages;
-          if (!wait_or_abort(&ms->kv_empty[s], (n & 1) ^ 1, ms, p)) break;
           uint8_t* st = smem + C::kOffStages + s * C::kStageStride;
-          mbar_arrive_expect_tx(&ms->kv_full[s], kStageBytes);
+          // pool rows of the tile's two 64-key halves
+          int y[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int kk = k0 + 64 * h;
-            int y = total_rows;  // fully out of range: TMA fills zeros
+            y[h] = total_rows;  // fully out of range: TMA fills zeros
             if (kk < un.key_hi) {
               const int lp = kk / p.page_size;
               const int phys = p.page_table[(int64_t)un.b * p.pt_stride + lp];
               if (phys >= 0 && phys < p.num_pages)
-                y = phys * p.page_size + (kk % p.page_size);
+                y[h] = phys * p.page_size + (kk % p.page_size);
               else
                 report(ms, MLA_ERR_BOUNDS);
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d_hint(st + c * kChunkBytes + h * 8192, &map_main, c * 128, y,
-                               &ms->kv_full[s], read_once);
-            tma_load_2d_hint(st + C::kTail + h * 4096, &map_tail, 0, y, &ms->kv_full[s], read_once);
           }
+          bool ok = true;
+#pragma unroll
+          for (int c = 0; c < 5; ++c) {  // chunks 0..3, then the tail
+            const int part = c < 4 ? part_of_chunk(c) : kTailPart;
+            uint64_t* full = &ms->kv_full[s][part];
+            if (c == 0 || c == 2) {  // a half begins
+              if (!(ok = wait_or_abort(&ms->kv_free[s][part], (n & 1) ^ 1, ms, p))) break;
+              mbar_arrive_expect_tx(full, part_bytes(part));
+            }
+            if (c < 4) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d_hint(st + c * kChunkBytes + h * 8192, &map_main, c * 128, y[h], full,
+                                 read_once);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d_hint(st + C::kTail + h * 4096, &map_tail, 0, y[h], full, read_once);
+            }
+          }
+          if (!ok) break;
           ++fill;
           prefetch_upto(fill + kPrefetchTiles);
         }
       }
-      // Drain: wait (bounded) until the consumer released every stage still holding a load.
-      for (uint32_t f = (fill > kStages ? fill - kStages : 0); f < fill; ++f) {
-        mbar_wait(&ms->kv_empty[f % kStages], (f / kStages) & 1, kWaitLimitNs);
-      }
+      // Drain: wait (bounded) until the consumers released every part still holding a load.
+      for (uint32_t f = (fill > kStages ? fill - kStages : 0); f < fill; ++f)
+        for (int c = 0; c < kParts; ++c)
+          mbar_wait(&ms->kv_free[f % kStages][c], (f / kStages) & 1, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ scores issuer
-    // QK of every tile, as soon as its KV stage is full, its S^T buffer has been read and
-    // its unit's query terms are staged. Values (PV) have their own issuing warp: a single
-    // thread spends tens of cycles per tcgen05.mma, so one issuer would serialise the two.
+    // QK of every tile, chunk by chunk as its KV stage fills, once its S^T buffer has been
+    // read and its unit's query terms are staged. Values (PV) have their own issuing warp: a
+    // single thread spends tens of cycles per tcgen05.mma, so one issuer would serialise the
+    // two.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = instr_desc(0, 0, 0, 0, 128, C::NQK);
       const uint64_t a_main0 = smem_desc(smem_addr(smem + C::kOffStages), 16, 1024, Swizzle::k128B);
@@ -708,18 +736,24 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const uint32_t qoff = (uint32_t)(qslot * C::kQBytes) >> 4;
         for (int t = 0; t < n; ++t, ++g) {
           const int s = g % kStages, sb = g % C::kSBuf;
-          if (!(ok = wait_or_abort(&ms->kv_full[s], (g / kStages) & 1, ms, p))) break;
+          const uint32_t ph = (g / kStages) & 1;
           if (!(ok = wait_or_abort(&ms->s_empty[sb], ((g / C::kSBuf) & 1) ^ 1, ms, p))) break;
-          tc_fence_after();
           const uint32_t soff = (uint32_t)(s * C::kStageStride) >> 4;
           const uint32_t d = tmem + C::kSCol + sb * C::NQK;
+          // each latent chunk as soon as it has landed, then the RoPE tail
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4 && ok; ++c) {
+            if (c == 0 || c == 2) {  // a half has landed
+              if (!(ok = wait_or_abort(&ms->kv_full[s][part_of_chunk(c)], ph, ms, p))) break;
+              tc_fence_after();
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_f8f6f4(d, a_main0 + soff + ((c * kChunkBytes + kk * 32) >> 4),
                          b_main0 + qoff + ((c * (C::NQK * 128) + kk * 32) >> 4), idesc_qk,
                          (c | kk) != 0);
+          }
+          if (!ok) break;  // the tail belongs to the second half, landed by now
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
             mma_f8f6f4(d, a_tail0 + soff + ((kk * 32) >> 4), b_tail0 + qoff + ((kk * 32) >> 4),
@@ -734,7 +768,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   } else if (warp == 3) {
     // ------------------------------------------------------------------ values issuer
     // PV of every tile the moment its probabilities are in shared memory; completion hands
-    // the KV stage back to the producer and lets the softmax reuse P and rescale O.
+    // the KV stage back to the producer, part by part, and lets the softmax reuse P and
+    // rescale O.
     if (lane == 0) {
       // A = V^T as e4m3 codes, B = P^T as e5m2 terms (kind::f8f6f4 takes each operand's
       // format from its own descriptor field), both MN-major
@@ -754,27 +789,29 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           const int s = g % kStages;
           const uint32_t soff = (uint32_t)(s * C::kStageStride) >> 4;
           const uint32_t poff = C::kPInStage ? soff : 0u;
-          // consecutive MMAs go to different dv chunks' accumulators where they can
+          // chunk by chunk, each freed for the next tile's load once its own MMAs complete
+          // (back-to-back MMAs into one accumulator cost no more than alternating ones)
+          // chunk by chunk (back-to-back MMAs into one accumulator cost no more than
+          // alternating ones); each half of the stage is handed back once its MMAs complete.
+          // The second half's release also stands for the whole tile's values being done
+          // (P, which lives in the tail at 48 rows, and O for the softmax's rescale).
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
+          for (int c = 0; c < 4; ++c) {
 #pragma unroll
-            for (int term = 0; term < 3; ++term) {
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t a = a0 + soff + ((c * kChunkBytes + ks * 4096) >> 4);
+              if (C::oterms(c) == 3) {  // stacked: one MMA over all three terms' rows
+                mma_f8f6f4(tmem + C::ocol(c), a, b0 + poff + ((ks * 512) >> 4), idesc_stacked,
+                           t > 0 || ks > 0);
+              } else {  // summed: one MMA per term into the same accumulator
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint64_t a = a0 + soff + ((c * kChunkBytes + ks * 4096) >> 4);
-                if (C::oterms(c) == 3) {  // stacked: one MMA over all three terms' rows
-                  if (term == 0)
-                    mma_f8f6f4(tmem + C::ocol(c), a, b0 + poff + ((ks * 512) >> 4), idesc_stacked,
-                               t > 0 || ks > 0);
-                } else {  // summed: one MMA per term into the same accumulator
+                for (int term = 0; term < 3; ++term)
                   mma_f8f6f4(tmem + C::ocol(c), a, b0 + poff + ((C::pterm(term) + ks * 512) >> 4),
                              idesc_term, t > 0 || ks > 0 || term > 0);
-                }
               }
             }
+            if (c == 1 || c == 3) mma_commit(&ms->kv_free[s][part_of_chunk(c)]);
           }
-          mma_commit(&ms->kv_empty[s]);
-          mma_commit(&ms->pv_done[g & 1]);
         }
       }
     }
@@ -833,7 +870,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     int pv_seen = -1;
     auto wait_pv_upto = [&](int target) -> bool {
       for (int g = pv_seen + 1; g <= target; ++g) {
-        if (!wait_or_abort(&ms->pv_done[g & 1], (g >> 1) & 1, ms, p)) return false;
+        if (!wait_or_abort(&ms->kv_free[g % kStages][kParts - 1], (g / kStages) & 1, ms, p)) return false;
         pv_seen = g;
       }
       return true;
@@ -1058,31 +1095,34 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int NT = C::oterms(c);
-        float o[3][RH];
 #pragma unroll
-        for (int term = 0; term < 3; ++term)
+        for (int cc = 0; cc < RH; cc += 8) {
+          if (rb + cc >= R) break;
+          // The rows' output offsets go to registers before any of these stores: as far as
+          // the compiler knows a store may alias the table, so a lookup between two stores
+          // would wait for the first one to drain (about 60 ns a store when every SM writes).
+          int roffs[8];
 #pragma unroll
-          for (int cc = 0; cc < RH; cc += 8) {
-            if (term >= NT) break;
-            float v[8];
-            tmem_ld8(tmem + lane_addr + C::ocol(c) + term * RP + rb + cc, v);
+          for (int e = 0; e < 8; ++e) roffs[e] = ms->row_off[rb + cc + e];
+          float o[3][8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[term][cc + e] = v[e];
-          }
-        tmem_wait_ld();
+          for (int term = 0; term < 3; ++term)
+            if (term < NT) tmem_ld8(tmem + lane_addr + C::ocol(c) + term * RP + rb + cc, o[term]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < RH; ++r) {
-          if (rb + r >= R) break;
-          float acc = o[0][r];
+          for (int e = 0; e < 8; ++e) {
+            const int r = cc + e;
+            if (rb + r >= R) break;
+            float acc = o[0][e];
 #pragma unroll
-          for (int term = 1; term < 3; ++term)
-            if (term < NT) acc += o[term][r];
-          const int dv = c * 128 + i;
-          const int roff = ms->row_off[rb + r];
-          if (final_out) {
-            store_out(p, ((int64_t)un.qrow0 + roff) * kDV + dv, acc * inv[r]);
-          } else {
-            p.part_out[((int64_t)un.slot * p.R + roff) * kDV + dv] = acc * inv[r];
+            for (int term = 1; term < 3; ++term)
+              if (term < NT) acc += o[term][e];
+            const int dv = c * 128 + i;
+            if (final_out) {
+              store_out(p, ((int64_t)un.qrow0 + roffs[e]) * kDV + dv, acc * inv[r]);
+            } else {
+              p.part_out[((int64_t)un.slot * p.R + roffs[e]) * kDV + dv] = acc * inv[r];
+            }
           }
         }
       }

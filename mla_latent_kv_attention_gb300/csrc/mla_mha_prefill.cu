@@ -45,6 +45,7 @@ constexpr int kBM = 128;                       // new positions per unit
 constexpr int kBox = 128 * 128;                // one 64-wide 16-bit box of 128 rows (16 KB)
 constexpr int kQBytes = 3 * kBox;              // q: dims 0..63, 64..127, 128..191
 constexpr int kStages = 2;                     // key ring and value ring, two buffers each
+static_assert(kStages == 2, "s_full / pv_done double as the rings' release barriers");
 constexpr int kThreads = 384;                  // warp 0 TMA (q, keys), 1 MMA, 2 TMA (values), 4..11 softmax
 constexpr uint32_t kTmemCols = 512;            // S0 at 0, S1 at 128; O0 at 256, O1 at 384
 constexpr uint32_t kColO = 256;
@@ -73,9 +74,10 @@ struct MhaCfg {
 constexpr float kRescale = 8.f;                // log2 growth of a row maximum that forces a rescale
 
 struct Misc {
-  // keys are released when their scores MMA completes, values when their values MMA does,
-  // so the next keys load while a tile's softmax runs
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  // keys are released when their scores MMA completes (s_full), values when their values
+  // MMA does (pv_done), so the next keys load while a tile's softmax runs. One commit
+  // serves both waiters: every tcgen05.commit costs the issuing thread time.
+  uint64_t k_full[kStages], v_full[kStages];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t q_full, q_free;
   uint64_t pair_bar;  // bounded barrier of the two softmax warpgroups (256 arrivals)
@@ -244,9 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ms->k_full[s], 1);
-      mbar_init(&ms->k_empty[s], 1);
       mbar_init(&ms->v_full[s], 1);
-      mbar_init(&ms->v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->s_full[i], 1);
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = wk.j0; j < wk.j1; ++j, ++g) {
           const int s = g & 1;
-          if (g >= 2 && !(ok = wait_or_abort(&ms->k_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
+          if (g >= 2 && !(ok = wait_or_abort(&ms->s_full[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* kb = smem + C::kOffK + s * C::kKBytes;
           mbar_arrive_expect_tx(&ms->k_full[s], C::kKBytes);
           const int n0 = j * kBN;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit& x = wk.x;
         for (int j = wk.j0; j < wk.j1; ++j, ++g) {
           const int s = g & 1;
-          if (g >= 2 && !(ok = wait_or_abort(&ms->v_empty[s], ((g >> 1) & 1) ^ 1, ms))) break;
+          if (g >= 2 && !(ok = wait_or_abort(&ms->pv_done[s], ((g >> 1) & 1) ^ 1, ms))) break;
           uint8_t* vb = smem + C::kOffV + s * C::kVBytes;
           mbar_arrive_expect_tx(&ms->v_full[s], C::kVBytes);
           tma_load_3d(vb, &map_kv, C::kValCol, x.h, j * kBN, &ms->v_full[s]);
@@ -341,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = smem_desc(v_addr + ks * 2048, C::kKBox, 1024, Swizzle::k128B);
           mma_f16_tmem_a(ocol, pcol + ks * 8, b, idesc_pv, (first && ks == 0) ? 0u : 1u);
         }
-        mma_commit(&ms->v_empty[gx & 1]);
         mma_commit(&ms->pv_done[gx & 1]);
         return true;
       };
@@ -369,7 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(tmem + s * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&ms->s_full[s]);
-          mma_commit(&ms->k_empty[s]);
           if (j == n - 1) mma_commit(&ms->q_free);
           if (j >= 1 && !(ok = pv(g - 1, j <= 2))) break;
         }
