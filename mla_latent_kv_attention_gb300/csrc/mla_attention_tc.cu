@@ -473,11 +473,11 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->s_full[s], 1);
-      mbar_init(&ms->s_empty[s], 128 * C::kNWG);
+      mbar_init(&ms->s_empty[s], 4 * C::kNWG);  // one arrival per softmax warp
     }
-    for (int w = 0; w < C::kNWG; ++w) mbar_init(&ms->wg_bar[w], 128);
-    mbar_init(&ms->p_full[0], 128 * C::kNWG);
-    mbar_init(&ms->p_full[1], 128 * C::kNWG);
+    for (int w = 0; w < C::kNWG; ++w) mbar_init(&ms->wg_bar[w], 4);
+    mbar_init(&ms->p_full[0], 4 * C::kNWG);
+    mbar_init(&ms->p_full[1], 4 * C::kNWG);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ms->q_full[s], 1);
       mbar_init(&ms->q_empty[s], 1);
@@ -867,19 +867,33 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     uint32_t tile = 0, wg_phase = 0, k = 0;  // k: units with work, in order
     // PV completions are confirmed in tile order, each before the PV two tiles later can
     // complete (that one needs this warpgroup's next P), so a phase parity names one tile
+    // A wait that gives up does not make its lane leave on its own: `ok` collects the
+    // outcome and the warp votes at fixed points (once a tile, before the epilogue), so a
+    // timeout never splits a warp ahead of a warp-wide instruction (tcgen05.ld, __syncwarp).
+    // After a failed wait the lanes run on to the vote on whatever they read; the call
+    // reports MLA_ERR_TIMEOUT and its outputs are not to be used.
+    // Arrivals are one per warp: the lanes meet at __syncwarp first (which also orders
+    // their earlier memory accesses before lane 0's release).
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return wait_or_abort(bar, parity, ms, p);
+    };
+    auto warp_arrive = [&](uint64_t* bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
     int pv_seen = -1;
     auto wait_pv_upto = [&](int target) -> bool {
       for (int g = pv_seen + 1; g <= target; ++g) {
-        if (!wait_or_abort(&ms->kv_free[g % kStages][kParts - 1], (g / kStages) & 1, ms, p)) return false;
+        if (!warp_wait(&ms->kv_free[g % kStages][kParts - 1], (g / kStages) & 1)) return false;
         pv_seen = g;
       }
       return true;
     };
     uint64_t* wg_bar = &ms->wg_bar[wg];
-    // Bounded warpgroup barrier: every thread arrives, then waits for the phase.
+    // Bounded warpgroup barrier: every warp arrives, then waits for the phase.
     auto wg_sync = [&]() -> bool {
-      mbar_arrive(wg_bar);
-      const bool good = wait_or_abort(wg_bar, wg_phase & 1, ms, p);
+      warp_arrive(wg_bar);
+      const bool good = warp_wait(wg_bar, wg_phase & 1);
       ++wg_phase;
       return good;
     };
@@ -907,7 +921,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       const int lim_cap = un.key_hi - 1;
       const int lim0 = min(lim_cap, L - p.n_q + un.j0 + p.mask_shift);
       // this unit's row scales (staged with its query terms)
-      if (!(ok = wait_or_abort(&ms->q_full[k % C::kQB], (k / C::kQB) & 1, ms, p))) break;
+      ok &= warp_wait(&ms->q_full[k % C::kQB], (k / C::kQB) & 1);
       float rs[RH], m[RH], l[RH];
 #pragma unroll
       for (int r = 0; r < RH; ++r) {
@@ -920,7 +934,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const int s = tile % kStages;
         const int k0 = un.key_lo + t * kTileKeys;
         const int kabs = k0 + i;
-        if (!(ok = wait_or_abort(&ms->s_full[sb], (tile / C::kSBuf) & 1, ms, p))) break;
+        ok &= warp_wait(&ms->s_full[sb], (tile / C::kSBuf) & 1);
         tc_fence_after();
         float x[RH];
         {
@@ -936,7 +950,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&ms->s_empty[sb]);
+        warp_arrive(&ms->s_empty[sb]);
         if (trace && threadIdx.x == 32 * kSoftmaxWarp0 && t == 0) {
           if (tile == 0) trace[kTrFirstScores] = globaltimer_ns();
           if (k == 1) trace[kTrUnit2Scores] = globaltimer_ns();
@@ -957,8 +971,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
         for (int r = 0; r < RH; ++r) over |= (x[r] > m[r] + kRescaleGap);
         over = __any_sync(0xffffffffu, over);
+        if (__any_sync(0xffffffffu, !ok)) {  // the warp's once-a-tile vote on its waits
+          ok = false;
+          break;
+        }
         if (lane == 0) ms->grow[tile & 1][wg * 4 + wq] = over ? 1 : 0;
-        if (!(ok = wg_sync())) break;
+        ok &= wg_sync();
         const int4 gf = *reinterpret_cast<const int4*>(&ms->grow[tile & 1][wg * 4]);
         bool need_rescale = false;
         float moff[RH];
@@ -970,7 +988,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             const float v = warp_max(x[r]);
             if (lane == 0) red[(rb + r) * 4 + wq] = v;
           }
-          if (!(ok = wg_sync())) break;
+          ok &= wg_sync();
 #pragma unroll
           for (int r = 0; r < RH; ++r) {
             const float4 t4 = *reinterpret_cast<const float4*>(&red[(rb + r) * 4]);
@@ -1019,7 +1037,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         // done (this tile's keys replaced its stage) and is only confirmed here.
         {
           const int upto = (int)tile - ((C::kPInStage && !need_rescale) ? 2 : 1);
-          if (!(ok = wait_pv_upto(upto))) break;
+          ok &= wait_pv_upto(upto);
           tc_fence_after();
         }
         if (t > 0) {
@@ -1069,9 +1087,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&ms->p_full[tile & 1]);
+        warp_arrive(&ms->p_full[tile & 1]);
       }
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       if (trace && threadIdx.x == 32 * kSoftmaxWarp0) trace[kTrLastP] = globaltimer_ns();
       // ---- epilogue: row sums, then O / l
 #pragma unroll
@@ -1080,7 +1101,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) ms->lred[wq][rb + r] = v;
       }
-      if (!(ok = wg_sync())) break;
+      ok &= wg_sync();
       float inv[RH];
 #pragma unroll
       for (int r = 0; r < RH; ++r) {
@@ -1089,7 +1110,11 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         l[r] = lt;
         inv[r] = lt > 0.f ? kv_scale / lt : 0.f;
       }
-      if (!(ok = wait_pv_upto((int)tile - 1))) break;
+      ok &= wait_pv_upto((int)tile - 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       if (trace && threadIdx.x == 32 * kSoftmaxWarp0) trace[kTrLastPV] = globaltimer_ns();
 #pragma unroll
