@@ -634,12 +634,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       // Prefill re-reads the same rows for every unit and keeps the default policy.
       const uint64_t read_once = args.prefill ? l2_policy_evict_normal() : l2_policy_evict_first();
       // L2 prefetch cursor: runs kPrefetchTiles tiles ahead of the TMA loads so that they
-      // find their pages in L2 (deeper than the two shared-memory stages allow).
+      // find their pages in L2 (deeper than the two shared-memory stages allow). The first
+      // kStages tiles are the TMA loads' own: the cursor starts past them (no page-table
+      // reads there: each is a round trip the second tile's load would wait behind).
       Cursor pf_c = first_unit(args, ms);
       UnitInfo pu = has_unit(args, ms, pf_c) ? unit_info(args, ms, pf_c) : UnitInfo{};
       int pf_k = pu.key_lo;
       uint32_t pf_tiles = 0;
-      auto prefetch_upto = [&](uint32_t target) {
+      auto prefetch_upto = [&](uint32_t target, bool issue) {
         while (pf_tiles < target && has_unit(args, ms, pf_c)) {
           if (pf_k >= pu.key_hi) {  // unit done (or empty)
             pf_c = next_unit(args, pf_c);
@@ -647,7 +649,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             pf_k = pu.key_lo;
             continue;
           }
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2 && issue; ++h) {
             const int kk = pf_k + 64 * h;
             if (kk < pu.key_hi) {
               const int phys = p.page_table[(int64_t)pu.b * p.pt_stride + kk / p.page_size];
@@ -662,6 +664,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           pf_k += kTileKeys;
         }
       };
+      prefetch_upto(kStages, false);
       for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && !aborted(ms) && !p.test_stall;
            cu = next_unit(args, cu)) {
         const UnitInfo un = unit_info(args, ms, cu);
@@ -706,7 +709,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           }
           if (!ok) break;
           ++fill;
-          prefetch_upto(fill + kPrefetchTiles);
+          prefetch_upto(fill + kPrefetchTiles, true);
         }
       }
       // Drain: wait (bounded) until the consumers released every part still holding a load.
