@@ -18,6 +18,14 @@
 // through distributed shared memory, and every CTA selects the bin on the totals. Selection
 // stops early when the bin that holds the k-th largest entry is kept whole. The kept sum is
 // a reduction in the output pass.
+//
+// After the first pass the selected bin usually holds a few dozen entries of the row. When
+// it holds at most kCandCap, the cluster skips the remaining passes: every CTA sends the
+// bin's entries (their bit patterns) to rank 0, with the sum of its own entries above the
+// bin; rank 0 finds the k-th largest among them by two local 10-bit radix passes, adds the
+// kept entries of the bin (they share one exponent, so their significands add exactly as
+// integers, in any order) to the sums from above the bin, and hands the pivot and the
+// reciprocal of the kept sum to every CTA: three cluster barriers in all, no kept-sum round.
 #include <cuda_runtime.h>
 
 #include "mla_internal.cuh"
@@ -33,6 +41,7 @@ constexpr int kTkMaxCluster = 8;
 constexpr int kBins = 2048;
 constexpr int kWarps = kTkThreads / 32;
 constexpr int kPasses = 3;
+constexpr int kCandCap = 2 * kBins;  // candidates rank 0 can hold (in the histograms of passes 2, 3)
 // digit width of a pass, below the sign bit (always 0 in a key): bits 30..20, 19..9, 8..0
 __device__ constexpr int digit_width(int pass) { return pass == kPasses - 1 ? 9 : 11; }
 
@@ -44,6 +53,13 @@ struct __align__(16) TkSmem {
   float part;                     // this CTA's kept sum (read by the other CTAs)
   int bin;
   unsigned above, in_bin;
+  // candidate path: rank 0's slot counter and the CTAs' sums above the bin (written by
+  // every CTA into rank 0), the pivot and reciprocal rank 0 hands out, a slot base
+  unsigned cand_n, cand_base;
+  float above_part[kTkMaxCluster];
+  unsigned b_pivot;
+  float b_inv;
+  unsigned long long sig_w[kWarps];
 };
 
 // Largest bin b with count(bins >= b) >= k, from the totals: writes b, the count of the
@@ -87,6 +103,122 @@ __device__ __forceinline__ float block_sum(TkSmem& s, float v) {
   return t;
 }
 
+// Exclusive prefix of `v` over the CTA (thread order); the CTA's total goes to *total.
+__device__ __forceinline__ unsigned block_excl_scan(TkSmem& s, unsigned v, unsigned* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s.wsum[warp] = incl;
+  __syncthreads();
+  unsigned before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    before += w < warp ? s.wsum[w] : 0u;
+    all += s.wsum[w];
+  }
+  *total = all;
+  return before + incl - v;
+}
+
+// The candidate path (see the top of the file). bin: the 12 high bits (sign bit, always 0,
+// then bits 30..20) every candidate shares; k: the rank sought among the bin's entries
+// (1-based, from the largest). Returns the pivot; *inv_out = 1 / (sum of the kept entries).
+template <typename TailKey>
+__device__ unsigned candidate_select(TkSmem& s, const unsigned (&key)[kTkPerThread], int64_t tail0,
+                                     int64_t tail_step, int lane, int V, TailKey tail_key, unsigned rank,
+                                     int n, unsigned bin, unsigned k, float* inv_out) {
+  const int t = threadIdx.x;
+  // this CTA's candidates and its sum above the bin
+  unsigned cnt = 0;
+  float above = 0.f;
+#pragma unroll
+  for (int j = 0; j < kTkPerThread; ++j) {
+    const unsigned hi = key[j] >> 20;
+    cnt += hi == bin;
+    if (hi > bin) above += __uint_as_float(key[j]);
+  }
+  for (int64_t i = tail0 + lane; i < V; i += tail_step) {
+    const unsigned kv = tail_key(i);
+    cnt += (kv >> 20) == bin;
+    if ((kv >> 20) > bin) above += __uint_as_float(kv);
+  }
+  unsigned mine_total;
+  const unsigned off = block_excl_scan(s, cnt, &mine_total);
+  above = block_sum(s, above);
+  if (t == 0) {
+    s.cand_base = sm100::atomic_add_dsmem_u32(&s.cand_n, 0, mine_total);
+    sm100::st_dsmem_u32(&s.above_part[rank], 0, __float_as_uint(above));
+  }
+  __syncthreads();
+  unsigned* cand = &s.hist[1][0];  // in rank 0: kCandCap slots
+  unsigned pos = s.cand_base + off;
+#pragma unroll
+  for (int j = 0; j < kTkPerThread; ++j)
+    if ((key[j] >> 20) == bin) sm100::st_dsmem_u32(cand + pos++, 0, key[j]);
+  for (int64_t i = tail0 + lane; i < V; i += tail_step) {
+    const unsigned kv = tail_key(i);
+    if ((kv >> 20) == bin) sm100::st_dsmem_u32(cand + pos++, 0, kv);
+  }
+  sm100::cluster_sync();  // rank 0 holds every candidate and every sum above the bin
+  if (rank == 0) {
+    const unsigned nc = s.cand_n;
+    unsigned piv = bin << 20;
+    unsigned pre = 0;  // selected bits 19..10
+    // two local passes of 10 bits: bits 19..10, then 9..0 of the entries still in play
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = pass == 0 ? 10 : 0;
+      for (int b = t; b < 1024; b += kTkThreads) s.tot[b] = 0u;
+      __syncthreads();
+      for (unsigned c = t; c < nc; c += kTkThreads) {
+        const unsigned kv = cand[c];
+        if (pass == 0 || ((kv >> 10) & 1023u) == pre) atomicAdd(&s.tot[(kv >> shift) & 1023u], 1u);
+      }
+      __syncthreads();
+      select_bin(s, k, 1024);
+      const unsigned b = (unsigned)s.bin, a = s.above, in = s.in_bin;
+      __syncthreads();  // s.bin / s.above / s.in_bin read before anything rewrites them
+      k -= a;
+      if (pass == 0) {
+        pre = b;
+        piv |= b << 10;
+        if (k == in) break;  // bin kept whole: its lowest pattern is the pivot
+      } else {
+        piv |= b;
+      }
+    }
+    // kept entries of the bin: one exponent, so the significands add exactly
+    const unsigned ex = bin >> 3;  // exponent field, bits 30..23
+    unsigned long long sig = 0;
+    for (unsigned c = t; c < nc; c += kTkThreads) {
+      const unsigned kv = cand[c];
+      if (kv >= piv) sig += (kv & 0x7FFFFFu) | (ex != 0 ? 0x800000u : 0u);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sig += __shfl_xor_sync(0xffffffffu, sig, o);
+    if (lane == 0) s.sig_w[t >> 5] = sig;
+    __syncthreads();
+    if (t == 0) {
+      unsigned long long sig_all = 0;
+      for (int w = 0; w < kWarps; ++w) sig_all += s.sig_w[w];
+      double total = ldexp((double)sig_all, (int)(ex != 0 ? ex : 1u) - 150);
+      for (int r = 0; r < n; ++r) total += (double)s.above_part[r];
+      const float inv = 1.f / (float)total;
+      for (int r = 0; r < n; ++r) {
+        sm100::st_dsmem_u32(&s.b_pivot, (uint32_t)r, piv);
+        sm100::st_dsmem_u32(&s.b_inv, (uint32_t)r, __float_as_uint(inv));
+      }
+    }
+  }
+  sm100::cluster_sync();  // every CTA has the pivot and the reciprocal
+  *inv_out = s.b_inv;
+  return s.b_pivot;
+}
+
 __global__ void __launch_bounds__(kTkThreads, 2)
     top_k_renorm_kernel(const float* __restrict__ probs, float* __restrict__ out, int V, int n,
                         const int32_t* __restrict__ top_k, int k_all) {
@@ -113,10 +245,13 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   };
   const int kk = top_k ? top_k[row] : k_all;
   unsigned pivot = 0;  // lowest kept bit pattern; 0 keeps everything
+  bool have_inv = false;  // the candidate path delivered 1 / (kept sum) with the pivot
+  float inv = 0.f;
   if (kk > 0 && kk < V) {
     // Zero entries past the end of the row only ever add zeros below a positive pivot, and
     // a pivot of zero keeps the zeros of the row anyway, so they change no selection.
     for (int b = t; b < kPasses * kBins; b += kTkThreads) (&s.hist[0][0])[b] = 0u;
+    if (t == 0) s.cand_n = 0u;
     __syncthreads();
     unsigned k = (unsigned)kk, prefix = 0;  // prefix: the selected high bits (sign bit first)
     int done = 1;
@@ -163,31 +298,38 @@ __global__ void __launch_bounds__(kTkThreads, 2)
         pivot = prefix << (32 - done);
         break;
       }
+      if (pass == 0 && s.in_bin <= (unsigned)kCandCap) {
+        pivot = candidate_select(s, key, tail0, tail_step, lane, V, tail_key, rank, n, prefix, k, &inv);
+        have_inv = true;
+        break;
+      }
       __syncthreads();  // s.bin / s.above / s.in_bin are read before the next pass writes them
     }
   }
-  float kept = 0.f;
+  if (!have_inv) {
+    float kept = 0.f;
 #pragma unroll
-  for (int j = 0; j < kTkPerThread; ++j)
-    if (key[j] >= pivot) kept += __uint_as_float(key[j]);
-  for (int64_t i = tail0 + lane; i < V; i += tail_step) {
-    const unsigned kv = tail_key(i);
-    if (kv >= pivot) kept += __uint_as_float(kv);
+    for (int j = 0; j < kTkPerThread; ++j)
+      if (key[j] >= pivot) kept += __uint_as_float(key[j]);
+    for (int64_t i = tail0 + lane; i < V; i += tail_step) {
+      const unsigned kv = tail_key(i);
+      if (kv >= pivot) kept += __uint_as_float(kv);
+    }
+    kept = block_sum(s, kept);
+    if (t == 0) s.part = kept;
+    sm100::cluster_sync();  // every CTA's part is written (and the last pass's reads are done)
+    float total = 0.f;
+#pragma unroll
+    for (int r0 = 0; r0 < kTkMaxCluster; r0 += 4) {
+      float parts[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        parts[r] = r0 + r < n ? __uint_as_float(sm100::ld_dsmem_u32(&s.part, (uint32_t)(r0 + r))) : 0.f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) total += parts[r];
+    }
+    inv = 1.f / total;
   }
-  kept = block_sum(s, kept);
-  if (t == 0) s.part = kept;
-  sm100::cluster_sync();  // every CTA's part is written (and the last pass's reads are done)
-  float total = 0.f;
-#pragma unroll
-  for (int r0 = 0; r0 < kTkMaxCluster; r0 += 4) {
-    float parts[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-      parts[r] = r0 + r < n ? __uint_as_float(sm100::ld_dsmem_u32(&s.part, (uint32_t)(r0 + r))) : 0.f;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) total += parts[r];
-  }
-  const float inv = 1.f / total;
 #pragma unroll
   for (int j = 0; j < kTkPerThread; ++j) {
     const int64_t i = base + (int64_t)j * kTkThreads;
@@ -197,7 +339,9 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     const unsigned kv = tail_key(i);
     __stcs(o + i, kv >= pivot ? __uint_as_float(kv) * inv : 0.f);
   }
-  sm100::cluster_sync();  // no CTA leaves while another may still read its shared memory
+  // no CTA leaves while another may still read its shared memory (the candidate path reads
+  // none after its last barrier)
+  if (!have_inv) sm100::cluster_sync();
 }
 
 }  // namespace

@@ -320,5 +320,21 @@ __device__ __forceinline__ uint4 ld_dsmem_v4(const void* p, uint32_t rank) {
   return v;
 }
 
+// Store a 32-bit word into the shared memory of CTA `rank` of this cluster, at the offset
+// that `p` has in this CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_u32(void* p, uint32_t rank, uint32_t v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
+// Atomic add to a 32-bit word in the shared memory of CTA `rank`; returns the old value.
+__device__ __forceinline__ uint32_t atomic_add_dsmem_u32(void* p, uint32_t rank, uint32_t v) {
+  uint32_t remote, old;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(remote), "r"(v) : "memory");
+  return old;
+}
+
 }  // namespace sm100
 }  // namespace mla
