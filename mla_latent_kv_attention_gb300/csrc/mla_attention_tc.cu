@@ -75,6 +75,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 11.0f;     // P carried as 2^(x - m + 11): at most 2^15 while x <= m + 4
 constexpr float kRescaleGap = 4.0f;  // the running max (log2 units) moves only past m + 4
 constexpr float kQTerm2 = 16.0f;     // the second query term carries the residual times 16
+constexpr float kNoMax = -1e30f;     // running max (less kPScale) of a row that has seen no key
 constexpr int kPrefetchTiles = 1;    // tiles the producer pulls into L2 ahead of its TMA loads
 
 template <int RP>
@@ -925,11 +926,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       const int lim0 = min(lim_cap, L - p.n_q + un.j0 + p.mask_shift);
       // this unit's row scales (staged with its query terms)
       ok &= warp_wait(&ms->q_full[k % C::kQB], (k / C::kQB) & 1);
-      float rs[RH], m[RH], l[RH];
+      // mo: the row's running max less kPScale (p = 2^(x - mo)); kNoMax before its first key
+      float rs[RH], mo[RH], l[RH];
 #pragma unroll
       for (int r = 0; r < RH; ++r) {
         rs[r] = ms->row_scale[k & 1][rb + r];
-        m[r] = -INFINITY;
+        mo[r] = kNoMax;
         l[r] = 0.f;
       }
       for (int t = 0; t < ntiles; ++t, ++tile) {
@@ -972,7 +974,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         // common case skips the exchange of per-row maxima.
         bool over = false;
 #pragma unroll
-        for (int r = 0; r < RH; ++r) over |= (x[r] > m[r] + kRescaleGap);
+        for (int r = 0; r < RH; ++r) over |= (x[r] > mo[r] + (kPScale + kRescaleGap));
         over = __any_sync(0xffffffffu, over);
         if (__any_sync(0xffffffffu, !ok)) {  // the warp's once-a-tile vote on its waits
           ok = false;
@@ -982,7 +984,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         ok &= wg_sync();
         const int4 gf = *reinterpret_cast<const int4*>(&ms->grow[tile & 1][wg * 4]);
         bool need_rescale = false;
-        float moff[RH];
         if ((gf.x | gf.y | gf.z | gf.w) != 0) {
           // tile max per row: warp max in hardware, then the four warps through shared memory
           float* red = &ms->red[tile & 1][0];
@@ -997,25 +998,23 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             const float4 t4 = *reinterpret_cast<const float4*>(&red[(rb + r) * 4]);
             const float tm = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
             float al = 1.f;
-            if (tm > m[r] + kRescaleGap) {  // lazy: small increases are absorbed by the headroom
-              al = ex2(m[r] - tm);  // 0 when m was -inf (nothing accumulated yet)
-              need_rescale |= (m[r] != -INFINITY);
+            if (tm > mo[r] + (kPScale + kRescaleGap)) {  // lazy: the headroom absorbs small increases
+              al = ex2(mo[r] + kPScale - tm);  // 0 before the first key (nothing accumulated yet)
+              need_rescale |= (mo[r] != kNoMax);
               l[r] *= al;
-              m[r] = tm;
+              mo[r] = tm - kPScale;
             }
             if (lane == 0) ms->alpha[rb + r] = al;
           }
         }
-#pragma unroll
-        for (int r = 0; r < RH; ++r) moff[r] = (m[r] == -INFINITY) ? 0.f : m[r] - kPScale;
         // p = 2^(x - m + 11) <= 2^15 rounded to fp16, then three e5m2 terms, each the
         // nearest e5m2 value to what the terms before it left (the differences are exact
         // in fp16); the row sum takes the float32 p
         uint32_t w1[RH / 4], w2[RH / 4], w3[RH / 4];
 #pragma unroll
         for (int r = 0; r < RH; r += 2) {
-          const float p0 = ex2(x[r] - moff[r]);
-          const float p1 = ex2(x[r + 1] - moff[r + 1]);
+          const float p0 = ex2(x[r] - mo[r]);  // masked (x = -inf) and keyless rows give 0
+          const float p1 = ex2(x[r + 1] - mo[r + 1]);
           l[r] += p0;
           l[r + 1] += p1;
           const uint32_t h = f32x2_to_f16x2(p0, p1);
@@ -1156,14 +1155,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       }
       tc_fence_before();
       if (i < RH && rb + i < R) {
-        float lt = 0.f, mm = -INFINITY;
+        float lt = 0.f, mm = kNoMax;
 #pragma unroll
         for (int r = 0; r < RH; ++r)
           if (r == i) {
             lt = l[r];
-            mm = m[r];
+            mm = mo[r];
           }
-        const float lse = (lt > 0.f) ? 0.6931471805599453f * (mm - kPScale + log2f(lt)) : -INFINITY;
+        const float lse = (lt > 0.f) ? 0.6931471805599453f * (mm + log2f(lt)) : -INFINITY;
         const int roff = ms->row_off[rb + i];
         if (final_out) {
           if (p.lse) p.lse[(int64_t)un.qrow0 + roff] = lse;
