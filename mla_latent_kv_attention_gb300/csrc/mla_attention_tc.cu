@@ -944,15 +944,16 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         float x[RH];
         {
           const uint32_t base = tmem + lane_addr + C::kSCol + sb * C::NQK + rb;
+          // every load of the tile first, one wait
+          float a[RH], b2[RH];
 #pragma unroll
           for (int c = 0; c < RH; c += 8) {
-            float a[8], b2[8];
-            tmem_ld8(base + c, a);
-            tmem_ld8(base + RP + c, b2);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[c + e] = fmaf(b2[e], 1.0f / kQTerm2, a[e]) * rs[c + e];
+            tmem_ld8(base + c, *reinterpret_cast<float(*)[8]>(&a[c]));
+            tmem_ld8(base + RP + c, *reinterpret_cast<float(*)[8]>(&b2[c]));
           }
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < RH; ++e) x[e] = fmaf(b2[e], 1.0f / kQTerm2, a[e]) * rs[e];
         }
         tc_fence_before();
         warp_arrive(&ms->s_empty[sb]);
