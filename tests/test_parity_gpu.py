@@ -266,13 +266,15 @@ def test_merge_lse_standalone():
 
 def test_merge_lse_many_partials():
     """More partials per row than the merge keeps in registers (256), few rows (narrow
-    chunks), and rows whose partials are all empty."""
+    chunks), rows whose partials are all empty, and a row whose only finite partials come
+    after empty ones past the first 256 (an empty piece there must add nothing, not NaN)."""
     g = torch.Generator().manual_seed(33)
-    S, R = 300, 3
+    S, R = 300, 4
     po = torch.randn(S, R, 512, generator=g)
     pl = torch.randn(S, R, generator=g) * 4
     pl[::7, 0] = -math.inf
     pl[:, 2] = -math.inf
+    pl[:288, 3] = -math.inf
     out, lse = mla.mla_merge_lse(po.to(DEV), pl.to(DEV))
     torch.cuda.synchronize()
     ref_out, ref_lse = oracle.merge_lse(po.double().numpy(), pl.double().numpy())
