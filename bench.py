@@ -413,6 +413,43 @@ def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
                      "launches_per_call": mla.mla_last_launch_count(),
                      "algorithmic_bytes": nbytes, "B": inp.B, "H": inp.H, "n_q": inp.n_q}
         del sets
+    # The headline decode as one layer of a model: eight layers back to back, each with its
+    # own 188 MB cache, queries, outputs and workspace, all sharing the step's page table and
+    # lengths (every layer of a decode step reads the same ones), captured in one CUDA graph.
+    # Each layer's attention kernel is a programmatic dependent of the merge before it, so
+    # its launch and prologue overlap that merge; the per-layer figure is a replay over 8.
+    inp = W.batched_paged_decode()
+    layers = 8
+    base = mla.KVCache.from_inputs(inp, dev)
+    chain = []
+    for li in range(layers):
+        kv = base if li == 0 else mla.KVCache(base.pool.clone(), base.page_table, base.seq_lens,
+                                              base.kv_scale)
+        q = inp.q[:, 0].contiguous().to(dev)
+        out = torch.empty(inp.B, inp.H, 512, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(inp.B, inp.H, dtype=torch.float32, device=dev)
+        ws = mla.workspace(mla.MLA_OP_DECODE, inp.B, inp.H, 1, dev)
+        chain.append((kv, q, out, lse, ws))
+
+    def layers_call(chain=chain, inp=inp):
+        for kv, q, out, lse, ws in chain:
+            mla.mla_decode(kv, q, inp.sm_scale, out=out, lse=lse, ws=ws)
+
+    layers_call()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_chain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_chain, stream=side):
+        layers_call()
+    torch.cuda.synchronize()
+    ms = _time_events(lambda i: g_chain.replay(), max(3, steps // 2), 3)
+    nbytes = accounting.decode_bytes(inp.seq_lens.tolist(), 1, inp.H)
+    gbs = nbytes / (ms / layers / 1e3) / 1e9
+    res["batched_paged_decode_8_layer_chain"] = {
+        "us_per_layer": ms * 1e3 / layers, "GB_s": gbs, "frac_of_hbm_peak": gbs / hbm_peak,
+        "layers": layers, "algorithmic_bytes_per_layer": nbytes}
+    del chain, base, g_chain
     inp = W.causal_prefill()
     kv = mla.KVCache.from_inputs(inp, dev)
     q = inp.q[0].contiguous().to(dev)

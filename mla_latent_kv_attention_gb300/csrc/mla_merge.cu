@@ -147,10 +147,13 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
 
 // Rows of the decode/verify path whose sequence was split over several CTAs, and rows of
 // sequences with no key at all (out = 0, lse = -inf). Launched as a programmatic dependent
-// of the attention kernel, whose grid it waits for.
+// of the attention kernel, whose grid it waits for; a following attention call launched
+// the same way may be scheduled from here on (its prologue overlaps this kernel, its inputs
+// are read only after this grid has completed).
 template <int VEC, typename OutT>
 __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t row = blockIdx.x;  // b * R + r
   const int chunk = blockIdx.y;
   const int b = (int)(row / p.R);
