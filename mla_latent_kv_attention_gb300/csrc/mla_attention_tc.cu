@@ -594,6 +594,66 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     }
     __syncthreads();
   }
+  // Loads of one key tile into its stage (producer thread): the two 64-key halves' pool rows
+  // from the page table, then the stage's two halves, each once the MMAs of the tile that
+  // held it have released it.
+  const int64_t rows64 = p.num_pages * (int64_t)p.page_size;
+  const int total_rows = rows64 > 0x7fffff00 ? 0x7fffff00 : (int)rows64;
+  auto issue_tile = [&](const UnitInfo& un, int k0, uint32_t fill, uint64_t policy) -> bool {
+    const int s = fill % kStages;
+    const uint32_t n = fill / kStages;
+    uint8_t* st = smem + C::kOffStages + s * C::kStageStride;
+    int y[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int kk = k0 + 64 * h;
+      y[h] = total_rows;  // fully out of range: TMA fills zeros
+      if (kk < un.key_hi) {
+        const int lp = kk / p.page_size;
+        const int phys = p.page_table[(int64_t)un.b * p.pt_stride + lp];
+        if (phys >= 0 && phys < p.num_pages)
+          y[h] = phys * p.page_size + (kk % p.page_size);
+        else
+          report(ms, MLA_ERR_BOUNDS);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 5; ++c) {  // chunks 0..3, then the tail
+      const int part = c < 4 ? part_of_chunk(c) : kTailPart;
+      uint64_t* full = &ms->kv_full[s][part];
+      if (c == 0 || c == 2) {  // a half begins
+        if (!wait_or_abort(&ms->kv_free[s][part], (n & 1) ^ 1, ms, p)) return false;
+        mbar_arrive_expect_tx(full, part_bytes(part));
+      }
+      if (c < 4) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_2d_hint(st + c * kChunkBytes + h * 8192, &map_main, c * 128, y[h], full, policy);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_2d_hint(st + C::kTail + h * 4096, &map_tail, 0, y[h], full, policy);
+      }
+    }
+    return true;
+  };
+  // Decode reads each cached row once per call: its lines should not push out of L2 what is
+  // reused (code, query rows, page tables, the partials the merge reads next). Prefill
+  // re-reads the same rows for every unit and keeps the default policy.
+  const uint64_t read_once = args.prefill ? l2_policy_evict_normal() : l2_policy_evict_first();
+  // The first unit's first tiles go out from here, straight after the plan: on the way to
+  // the producer's loop a cold kernel spends microseconds fetching instructions.
+  uint32_t early = 0;
+  if (threadIdx.x == 0 && !p.test_stall) {
+    const Cursor c0 = first_unit(args, ms);
+    if (has_unit(args, ms, c0)) {
+      const UnitInfo u0 = unit_info(args, ms, c0);
+      for (int k0 = u0.key_lo; k0 < u0.key_hi && early < (uint32_t)kStages; k0 += kTileKeys) {
+        if (!issue_tile(u0, k0, early, read_once)) break;
+        ++early;
+      }
+    }
+  }
   if (trace && threadIdx.x == 0) trace[kTrPlanned] = globaltimer_ns();
 
   // The first unit's queries are on every CTA's critical path: warps 2.. stage them into
@@ -627,13 +687,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int64_t rows64 = p.num_pages * (int64_t)p.page_size;
-      const int total_rows = rows64 > 0x7fffff00 ? 0x7fffff00 : (int)rows64;
-      uint32_t fill = 0;  // tiles issued so far
-      // Decode reads each cached row once per call: its lines should not push out of L2
-      // what is reused (code, query rows, page tables, the partials the merge reads next).
-      // Prefill re-reads the same rows for every unit and keeps the default policy.
-      const uint64_t read_once = args.prefill ? l2_policy_evict_normal() : l2_policy_evict_first();
+      uint32_t fill = 0;  // tiles issued so far (the first `early` ones in the prologue)
       // L2 prefetch cursor: runs kPrefetchTiles tiles ahead of the TMA loads so that they
       // find their pages in L2 (deeper than the two shared-memory stages allow). The first
       // kStages tiles are the TMA loads' own: the cursor starts past them (no page-table
@@ -670,44 +724,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
            cu = next_unit(args, cu)) {
         const UnitInfo un = unit_info(args, ms, cu);
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
-          const int s = fill % kStages;
-          const uint32_t n = fill / kStages;
-          uint8_t* st = smem + C::kOffStages + s * C::kStageStride;
-          // pool rows of the tile's two 64-key halves
-          int y[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int kk = k0 + 64 * h;
-            y[h] = total_rows;  // fully out of range: TMA fills zeros
-            if (kk < un.key_hi) {
-              const int lp = kk / p.page_size;
-              const int phys = p.page_table[(int64_t)un.b * p.pt_stride + lp];
-              if (phys >= 0 && phys < p.num_pages)
-                y[h] = phys * p.page_size + (kk % p.page_size);
-              else
-                report(ms, MLA_ERR_BOUNDS);
-            }
-          }
-          bool ok = true;
-#pragma unroll
-          for (int c = 0; c < 5; ++c) {  // chunks 0..3, then the tail
-            const int part = c < 4 ? part_of_chunk(c) : kTailPart;
-            uint64_t* full = &ms->kv_full[s][part];
-            if (c == 0 || c == 2) {  // a half begins
-              if (!(ok = wait_or_abort(&ms->kv_free[s][part], (n & 1) ^ 1, ms, p))) break;
-              mbar_arrive_expect_tx(full, part_bytes(part));
-            }
-            if (c < 4) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                tma_load_2d_hint(st + c * kChunkBytes + h * 8192, &map_main, c * 128, y[h], full,
-                                 read_once);
-            } else {
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                tma_load_2d_hint(st + C::kTail + h * 4096, &map_tail, 0, y[h], full, read_once);
-            }
-          }
+          const bool ok = fill < early || issue_tile(un, k0, fill, read_once);
           if (!ok) break;
           ++fill;
           prefetch_upto(fill + kPrefetchTiles, true);
