@@ -1094,16 +1094,32 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
         // P^T: MN-major, 16 rows x 8 keys core matrices; term t, row group g at
         // pterm(t) + g * 2048, key i at (i / 8) * 128 + (i % 8) * 16, row r at byte r % 16.
-        // This warpgroup writes its rows 8 at a time (8-byte halves of the 16-byte rows).
+        // A warpgroup with 16 rows (a whole row group) writes each key's 16 bytes at once: a
+        // warp then stores 512 contiguous bytes, free of bank conflicts (8-byte halves at a
+        // 16-byte stride took four shared-memory wavefronts a store where two suffice). With
+        // 8 rows it writes its 8-byte half.
         uint8_t* pb = C::kPInStage ? smem + C::kOffStages + s * C::kStageStride + 4 * kChunkBytes : pbuf;
         const int off = (i >> 3) * 128 + (i & 7) * 16;
+        if constexpr (RH % 16 == 0) {
 #pragma unroll
-        for (int blk = 0; blk < RH / 8; ++blk) {
-          const int row0 = rb + 8 * blk;
-          const int o = (row0 >> 4) * 2048 + off + ((row0 & 15) >> 3) * 8;
-          *reinterpret_cast<uint2*>(pb + C::pterm(0) + o) = make_uint2(w1[2 * blk], w1[2 * blk + 1]);
-          *reinterpret_cast<uint2*>(pb + C::pterm(1) + o) = make_uint2(w2[2 * blk], w2[2 * blk + 1]);
-          *reinterpret_cast<uint2*>(pb + C::pterm(2) + o) = make_uint2(w3[2 * blk], w3[2 * blk + 1]);
+          for (int blk = 0; blk < RH / 16; ++blk) {
+            const int o = ((rb >> 4) + blk) * 2048 + off;
+            *reinterpret_cast<uint4*>(pb + C::pterm(0) + o) =
+                make_uint4(w1[4 * blk], w1[4 * blk + 1], w1[4 * blk + 2], w1[4 * blk + 3]);
+            *reinterpret_cast<uint4*>(pb + C::pterm(1) + o) =
+                make_uint4(w2[4 * blk], w2[4 * blk + 1], w2[4 * blk + 2], w2[4 * blk + 3]);
+            *reinterpret_cast<uint4*>(pb + C::pterm(2) + o) =
+                make_uint4(w3[4 * blk], w3[4 * blk + 1], w3[4 * blk + 2], w3[4 * blk + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int blk = 0; blk < RH / 8; ++blk) {
+            const int row0 = rb + 8 * blk;
+            const int o = (row0 >> 4) * 2048 + off + ((row0 & 15) >> 3) * 8;
+            *reinterpret_cast<uint2*>(pb + C::pterm(0) + o) = make_uint2(w1[2 * blk], w1[2 * blk + 1]);
+            *reinterpret_cast<uint2*>(pb + C::pterm(1) + o) = make_uint2(w2[2 * blk], w2[2 * blk + 1]);
+            *reinterpret_cast<uint2*>(pb + C::pterm(2) + o) = make_uint2(w3[2 * blk], w3[2 * blk + 1]);
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
