@@ -222,6 +222,9 @@ __device__ __forceinline__ void store_out(const AttnParams& p, int64_t idx, floa
     p.out[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// PF: the launch is a prefill (units are blocks of new positions; no split plan). A
+// compile-time flag: the decode kernel then carries none of the prefill paths.
+template <bool PF>
 __device__ __forceinline__ Cursor first_unit(const DecodeArgs& a, const Misc* ms) {
   Cursor c;
   c.u = blockIdx.x;
@@ -231,14 +234,16 @@ __device__ __forceinline__ Cursor first_unit(const DecodeArgs& a, const Misc* ms
   return c;
 }
 
+template <bool PF>
 __device__ __forceinline__ bool has_unit(const DecodeArgs& a, const Misc* ms, const Cursor& c) {
-  return a.prefill ? c.u < a.num_units : (c.b < a.p.B && c.pre < ms->plan_x1);
+  return PF ? c.u < a.num_units : (c.b < a.p.B && c.pre < ms->plan_x1);
 }
 
 // The next unit: the next sequence with at least one key (decode/verify), or the next
 // unit index this CTA owns (prefill).
+template <bool PF>
 __device__ __forceinline__ Cursor next_unit(const DecodeArgs& a, Cursor c) {
-  if (a.prefill) {
+  if (PF) {
     c.u += gridDim.x;
     return c;
   }
@@ -251,10 +256,11 @@ __device__ __forceinline__ Cursor next_unit(const DecodeArgs& a, Cursor c) {
   return c;
 }
 
+template <bool PF>
 __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, const Misc* ms, const Cursor& c) {
   const AttnParams& p = a.p;
   UnitInfo x;
-  if (!a.prefill) {
+  if (!PF) {
     const long long nb = blocks_of(c.L);
     const long long blo = max(ms->plan_x0, c.pre), bhi = min(ms->plan_x1, c.pre + nb);
     x.b = c.b;
@@ -447,7 +453,7 @@ __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int
   }
 }
 
-template <int RP>
+template <int RP, bool PF>
 __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ DecodeArgs args,
                      const __grid_constant__ CUtensorMap map_main,
@@ -513,7 +519,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;");
   if (trace && threadIdx.x == 0) trace[kTrWaited] = globaltimer_ns();
 
-  if (!args.prefill) {
+  if (!PF) {
     // ---- split plan (decode/verify), computed by every CTA for itself. All sequences,
     // laid end to end on a cost axis (each as kUnitCost fixed units, then its 128-key
     // blocks), are cut into gridDim.x nearly equal contiguous ranges; this CTA owns
@@ -583,8 +589,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         prefetch_l2(reinterpret_cast<const uint8_t*>(
                         p.q + ((int64_t)b0 * p.R + ms->row_off[t / 9]) * kD) + (t % 9) * 128);
       // and the second unit's rows (its sequence follows b0) for the prologue's second pass
-      const Cursor c1 = next_unit(args, first_unit(args, ms));
-      if (t < qlines && has_unit(args, ms, c1))
+      const Cursor c1 = next_unit<PF>(args, first_unit<PF>(args, ms));
+      if (t < qlines && has_unit<PF>(args, ms, c1))
         prefetch_l2(reinterpret_cast<const uint8_t*>(
                         p.q + ((int64_t)c1.b * p.R + ms->row_off[t / 9]) * kD) + (t % 9) * 128);
       const int64_t pg0 = max(0ll, ms->plan_x0 - ms->plan_pre0) * kKeyBlock / p.page_size;
@@ -640,14 +646,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   // Decode reads each cached row once per call: its lines should not push out of L2 what is
   // reused (code, query rows, page tables, the partials the merge reads next). Prefill
   // re-reads the same rows for every unit and keeps the default policy.
-  const uint64_t read_once = args.prefill ? l2_policy_evict_normal() : l2_policy_evict_first();
+  const uint64_t read_once = PF ? l2_policy_evict_normal() : l2_policy_evict_first();
   // The first unit's first tiles go out from here, straight after the plan: on the way to
   // the producer's loop a cold kernel spends microseconds fetching instructions.
   uint32_t early = 0;
   if (threadIdx.x == 0 && !p.test_stall) {
-    const Cursor c0 = first_unit(args, ms);
-    if (has_unit(args, ms, c0)) {
-      const UnitInfo u0 = unit_info(args, ms, c0);
+    const Cursor c0 = first_unit<PF>(args, ms);
+    if (has_unit<PF>(args, ms, c0)) {
+      const UnitInfo u0 = unit_info<PF>(args, ms, c0);
       for (int k0 = u0.key_lo; k0 < u0.key_hi && early < (uint32_t)kStages; k0 += kTileKeys) {
         if (!issue_tile(u0, k0, early, read_once)) break;
         ++early;
@@ -663,18 +669,18 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   // second unit there before the first key tile lands, the stager warp each later one while
   // the unit before it runs.
   if (warp >= 2) {
-    Cursor c0 = first_unit(args, ms);
-    while (has_unit(args, ms, c0) && tiles_in(unit_info(args, ms, c0)) == 0) c0 = next_unit(args, c0);
-    if (has_unit(args, ms, c0)) {
-      const UnitInfo ui = unit_info(args, ms, c0);
+    Cursor c0 = first_unit<PF>(args, ms);
+    while (has_unit<PF>(args, ms, c0) && tiles_in(unit_info<PF>(args, ms, c0)) == 0) c0 = next_unit<PF>(args, c0);
+    if (has_unit<PF>(args, ms, c0)) {
+      const UnitInfo ui = unit_info<PF>(args, ms, c0);
       stage_rows<RP>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, qbuf,
                      ms->row_scale[0], warp - 2, C::kStageWarps, lane);
       fence_proxy_async_smem();
       mbar_arrive(&ms->q0_done);
-      Cursor c1 = next_unit(args, c0);
-      while (has_unit(args, ms, c1) && tiles_in(unit_info(args, ms, c1)) == 0) c1 = next_unit(args, c1);
-      if (has_unit(args, ms, c1)) {
-        const UnitInfo u1 = unit_info(args, ms, c1);
+      Cursor c1 = next_unit<PF>(args, c0);
+      while (has_unit<PF>(args, ms, c1) && tiles_in(unit_info<PF>(args, ms, c1)) == 0) c1 = next_unit<PF>(args, c1);
+      if (has_unit<PF>(args, ms, c1)) {
+        const UnitInfo u1 = unit_info<PF>(args, ms, c1);
         uint8_t* img = p.qimg + (int64_t)blockIdx.x * p.qimg_stride;
         stage_rows<RP>(p, u1.rows, ms->row_off, p.q + (int64_t)u1.qrow0 * kD, img,
                        reinterpret_cast<float*>(img + C::kQBytes), warp - 2, C::kStageWarps, lane);
@@ -692,15 +698,15 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       // find their pages in L2 (deeper than the two shared-memory stages allow). The first
       // kStages tiles are the TMA loads' own: the cursor starts past them (no page-table
       // reads there: each is a round trip the second tile's load would wait behind).
-      Cursor pf_c = first_unit(args, ms);
-      UnitInfo pu = has_unit(args, ms, pf_c) ? unit_info(args, ms, pf_c) : UnitInfo{};
+      Cursor pf_c = first_unit<PF>(args, ms);
+      UnitInfo pu = has_unit<PF>(args, ms, pf_c) ? unit_info<PF>(args, ms, pf_c) : UnitInfo{};
       int pf_k = pu.key_lo;
       uint32_t pf_tiles = 0;
       auto prefetch_upto = [&](uint32_t target, bool issue) {
-        while (pf_tiles < target && has_unit(args, ms, pf_c)) {
+        while (pf_tiles < target && has_unit<PF>(args, ms, pf_c)) {
           if (pf_k >= pu.key_hi) {  // unit done (or empty)
-            pf_c = next_unit(args, pf_c);
-            if (has_unit(args, ms, pf_c)) pu = unit_info(args, ms, pf_c);
+            pf_c = next_unit<PF>(args, pf_c);
+            if (has_unit<PF>(args, ms, pf_c)) pu = unit_info<PF>(args, ms, pf_c);
             pf_k = pu.key_lo;
             continue;
           }
@@ -720,9 +726,9 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
       };
       prefetch_upto(kStages, false);
-      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && !aborted(ms) && !p.test_stall;
-           cu = next_unit(args, cu)) {
-        const UnitInfo un = unit_info(args, ms, cu);
+      for (Cursor cu = first_unit<PF>(args, ms); has_unit<PF>(args, ms, cu) && !aborted(ms) && !p.test_stall;
+           cu = next_unit<PF>(args, cu)) {
+        const UnitInfo un = unit_info<PF>(args, ms, cu);
         for (int k0 = un.key_lo; k0 < un.key_hi; k0 += kTileKeys) {
           const bool ok = fill < early || issue_tile(un, k0, fill, read_once);
           if (!ok) break;
@@ -749,8 +755,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       const uint64_t b_tail0 = smem_desc(smem_addr(qbuf + 4 * (C::NQK * 128)), 16, 512, Swizzle::k64B);
       uint32_t g = 0, units_done = 0;
       bool ok = true;
-      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && ok; cu = next_unit(args, cu)) {
-        const int n = tiles_in(unit_info(args, ms, cu));
+      for (Cursor cu = first_unit<PF>(args, ms); has_unit<PF>(args, ms, cu) && ok; cu = next_unit<PF>(args, cu)) {
+        const int n = tiles_in(unit_info<PF>(args, ms, cu));
         if (n == 0) continue;
         const int qslot = units_done % C::kQB;
         if (!(ok = wait_or_abort(&ms->q_full[qslot], (units_done / C::kQB) & 1, ms, p))) break;
@@ -802,8 +808,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                                     128, 2048, Swizzle::kNone);
       uint32_t g = 0;
       bool ok = true;
-      for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && ok; cu = next_unit(args, cu)) {
-        const int n = tiles_in(unit_info(args, ms, cu));
+      for (Cursor cu = first_unit<PF>(args, ms); has_unit<PF>(args, ms, cu) && ok; cu = next_unit<PF>(args, cu)) {
+        const int n = tiles_in(unit_info<PF>(args, ms, cu));
         for (int t = 0; t < n; ++t, ++g) {
           if (!(ok = wait_or_abort(&ms->p_full[g & 1], (g >> 1) & 1, ms, p))) break;
           tc_fence_after();
@@ -844,8 +850,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     uint32_t k = 0;  // units with work, in order
     uint8_t* img = p.qimg + (int64_t)blockIdx.x * p.qimg_stride;
     constexpr uint32_t kImgBytes = C::kQBytes + 48 * sizeof(float);
-    for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu); cu = next_unit(args, cu)) {
-      const UnitInfo ui = unit_info(args, ms, cu);
+    for (Cursor cu = first_unit<PF>(args, ms); has_unit<PF>(args, ms, cu); cu = next_unit<PF>(args, cu)) {
+      const UnitInfo ui = unit_info<PF>(args, ms, cu);
       if (tiles_in(ui) == 0) continue;
       const int slot = k % C::kQB;
       if (k == 0) {  // staged into shared memory by warps 2.. in the prologue
@@ -919,8 +925,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       return good;
     };
     bool ok = true;
-    for (Cursor cu = first_unit(args, ms); has_unit(args, ms, cu) && ok; cu = next_unit(args, cu)) {
-      const UnitInfo un = unit_info(args, ms, cu);
+    for (Cursor cu = first_unit<PF>(args, ms); has_unit<PF>(args, ms, cu) && ok; cu = next_unit<PF>(args, cu)) {
+      const UnitInfo un = unit_info<PF>(args, ms, cu);
       const int R = un.rows;
       const int ntiles = tiles_in(un);
       const bool final_out = un.final_out != 0;
@@ -1275,11 +1281,11 @@ bool encode_pool_maps(const AttnParams& p, CUtensorMap* main_map, CUtensorMap* t
   return r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS;
 }
 
-template <int RP>
+template <int RP, bool PF>
 cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensorMap& mt,
                       int grid, cudaStream_t s) {
   constexpr int smem = smem_bytes<RP>();
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<RP>,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<RP, PF>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1292,7 +1298,7 @@ cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensor
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<RP>, a, mm, mt);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<RP, PF>, a, mm, mt);
 }
 
 }  // namespace
@@ -1318,11 +1324,11 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
     a.status_overwrite = (gi == 0);
     cudaError_t e;
     if (a.rows <= 16)
-      e = launch_rp<16>(a, mm, mt, grid, s);
+      e = launch_rp<16, false>(a, mm, mt, grid, s);
     else if (a.rows <= 32)
-      e = launch_rp<32>(a, mm, mt, grid, s);
+      e = launch_rp<32, false>(a, mm, mt, grid, s);
     else
-      e = launch_rp<48>(a, mm, mt, grid, s);
+      e = launch_rp<48, false>(a, mm, mt, grid, s);
     if (e != cudaSuccess) return e;
     ++*launches;
   }
@@ -1345,7 +1351,7 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, 
   a.status_overwrite = 1;
   a.num_units = (p.n_q + a.P - 1) / a.P;
   const int grid = min(num_sms, a.num_units);
-  const cudaError_t e = launch_rp<48>(a, mm, mt, grid, s);
+  const cudaError_t e = launch_rp<48, true>(a, mm, mt, grid, s);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
