@@ -453,7 +453,7 @@ __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int
   }
 }
 
-template <int RP, bool PF>
+template <int RP, bool PF, bool TR>
 __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ DecodeArgs args,
                      const __grid_constant__ CUtensorMap map_main,
@@ -468,8 +468,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
   uint8_t* qbuf = smem + C::kOffQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // profiling hook: this CTA's stamps, or null
-  unsigned long long* const trace =
-      (p.trace && (int)blockIdx.x < p.trace_ctas) ? p.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
+  // (TR: a separate instantiation for traced calls, so the usual one carries no stamp code)
+  unsigned long long* const trace = (TR && p.trace && (int)blockIdx.x < p.trace_ctas)
+                                        ? p.trace + (size_t)blockIdx.x * kTraceWords
+                                        : nullptr;
   if (trace && threadIdx.x == 0) trace[kTrEntry] = globaltimer_ns();
 
   if (threadIdx.x == 0) {
@@ -1281,11 +1283,11 @@ bool encode_pool_maps(const AttnParams& p, CUtensorMap* main_map, CUtensorMap* t
   return r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS;
 }
 
-template <int RP, bool PF>
-cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensorMap& mt,
-                      int grid, cudaStream_t s) {
+template <int RP, bool PF, bool TR>
+cudaError_t launch_rp_tr(const DecodeArgs& a, const CUtensorMap& mm, const CUtensorMap& mt,
+                         int grid, cudaStream_t s) {
   constexpr int smem = smem_bytes<RP>();
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<RP, PF>,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<RP, PF, TR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1298,7 +1300,14 @@ cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensor
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<RP, PF>, a, mm, mt);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<RP, PF, TR>, a, mm, mt);
+}
+
+template <int RP, bool PF>
+cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensorMap& mt,
+                      int grid, cudaStream_t s) {
+  return a.p.trace ? launch_rp_tr<RP, PF, true>(a, mm, mt, grid, s)
+                   : launch_rp_tr<RP, PF, false>(a, mm, mt, grid, s);
 }
 
 }  // namespace
