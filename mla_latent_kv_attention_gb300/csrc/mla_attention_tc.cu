@@ -112,6 +112,9 @@ struct Cfg {
   // 12 KB between the chunks and the tail, term 0 over the first 6 KB of the tail, which
   // the scores no longer need by then. Otherwise one P buffer serves every tile.
   static constexpr bool kPInStage = (RP == 48);
+  // dv-chunk loops of the epilogue and the rescale: rolled up at 16 rows (measured: smaller
+  // code, a faster decode), unrolled at 32 and 48 (rolled, they spill)
+  static constexpr int kUnrollChunks = (RP == 16) ? 1 : 4;
   static constexpr int kPTerm = (RP / 16) * 2048;       // one term: RP/16 groups of 16 rows
   static constexpr int kTail = 4 * kChunkBytes + (kPInStage ? 2 * kPTerm : 0);
   static constexpr int kStageStride = kTail + 2 * 4096;
@@ -1072,7 +1075,9 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
           if (need_rescale) {
             __syncwarp();
             const float* al = &ms->alpha[rb];
-#pragma unroll
+            // (rare: rolled up at 16 rows, so that the code of the tile loop stays small; at
+            // more rows the rolled loop needs more registers than there are)
+#pragma unroll(C::kUnrollChunks)
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
               for (int term = 0; term < C::oterms(c); ++term) {
@@ -1161,7 +1166,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       }
       tc_fence_after();
       if (trace && threadIdx.x == 32 * kSoftmaxWarp0) trace[kTrLastPV] = globaltimer_ns();
-#pragma unroll
+      // (once a unit: rolled up over the dv chunks at 16 rows, fewer instructions to fetch)
+#pragma unroll(C::kUnrollChunks)
       for (int c = 0; c < 4; ++c) {
         const int NT = C::oterms(c);
 #pragma unroll
