@@ -373,17 +373,20 @@ __device__ __forceinline__ int q_offset(int n, int w16) {
 // rounded: exact for entries down to 2^-14.8 of the row's largest magnitude, within
 // 2^-21.8 of it below), and the rows' score scales into row_scale[]. Rows at or past R are
 // written as zeros.
-template <int RP>
+template <int RP, int NW>
 __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int* row_off,
                                        const uint16_t* qseq, uint8_t* qdst, float* row_scale,
-                                       int w0, int nw, int lane) {
+                                       int w0, int lane) {
   using C = Cfg<RP>;
   const float kv_scale = p.kv_scale;
-  // rows r0, r0 + nw, r0 + 2 nw, r0 + 3 nw of this warp: all loads first, then the arithmetic
-  for (int r0 = w0; r0 < RP; r0 += 4 * nw) {
-    uint4 ld[4][2], tl[4][2];
+  constexpr int nw = NW;  // warps staging together
+  // rows of one pass of a warp (at most four; no more than NW warps leave for it)
+  constexpr int K2 = (RP + NW - 1) / NW < 4 ? (RP + NW - 1) / NW : 4;
+  // rows r0, r0 + nw, ... of this warp: all loads first, then the arithmetic
+  for (int r0 = w0; r0 < RP; r0 += K2 * nw) {
+    uint4 ld[K2][2], tl[K2][2];
 #pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
+    for (int k2 = 0; k2 < K2; ++k2) {
       const int r = r0 + nw * k2;
       ld[k2][0] = ld[k2][1] = tl[k2][0] = tl[k2][1] = make_uint4(0, 0, 0, 0);
       if (r < R) {
@@ -397,7 +400,7 @@ __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int
       }
     }
 #pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
+    for (int k2 = 0; k2 < K2; ++k2) {
       const int r = r0 + nw * k2;
       if (r >= RP) break;
       const bool real = r < R;
@@ -678,8 +681,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     while (has_unit<PF>(args, ms, c0) && tiles_in(unit_info<PF>(args, ms, c0)) == 0) c0 = next_unit<PF>(args, c0);
     if (has_unit<PF>(args, ms, c0)) {
       const UnitInfo ui = unit_info<PF>(args, ms, c0);
-      stage_rows<RP>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, qbuf,
-                     ms->row_scale[0], warp - 2, C::kStageWarps, lane);
+      stage_rows<RP, C::kStageWarps>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, qbuf,
+                                     ms->row_scale[0], warp - 2, lane);
       fence_proxy_async_smem();
       mbar_arrive(&ms->q0_done);
       Cursor c1 = next_unit<PF>(args, c0);
@@ -687,8 +690,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       if (has_unit<PF>(args, ms, c1)) {
         const UnitInfo u1 = unit_info<PF>(args, ms, c1);
         uint8_t* img = p.qimg + (int64_t)blockIdx.x * p.qimg_stride;
-        stage_rows<RP>(p, u1.rows, ms->row_off, p.q + (int64_t)u1.qrow0 * kD, img,
-                       reinterpret_cast<float*>(img + C::kQBytes), warp - 2, C::kStageWarps, lane);
+        stage_rows<RP, C::kStageWarps>(p, u1.rows, ms->row_off, p.q + (int64_t)u1.qrow0 * kD, img,
+                                       reinterpret_cast<float*>(img + C::kQBytes), warp - 2, lane);
         fence_proxy_async_global();
         mbar_arrive(&ms->q1_done);
       }
@@ -871,8 +874,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         // the image is free once the previous unit's copy out of it has landed
         const uint32_t pk = k - 1;
         if (!wait_or_abort(&ms->q_full[pk % C::kQB], (pk / C::kQB) & 1, ms, p)) break;
-        stage_rows<RP>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, img,
-                       reinterpret_cast<float*>(img + C::kQBytes), 0, 1, lane);
+        stage_rows<RP, 1>(p, ui.rows, ms->row_off, p.q + (int64_t)ui.qrow0 * kD, img,
+                          reinterpret_cast<float*>(img + C::kQBytes), 0, lane);
         fence_proxy_async_global();
         __syncwarp();
       }
