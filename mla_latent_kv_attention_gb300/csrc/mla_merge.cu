@@ -22,6 +22,7 @@ namespace {
 constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = 32 * kMergeWarps;
 
+
 // Merge one dv chunk (32 * VEC values; lane l owns VEC consecutive ones) of one row from
 // `count` partials; slot_of(i) gives the partial index of piece i, whose row sits at
 // po[(slot * R + r) * 512] and pl[slot * R + r]. Latency sets the cost (the partials were
@@ -34,18 +35,23 @@ __device__ __forceinline__ void store_val(uint16_t* p, float v) {
 }
 __device__ __forceinline__ void store_val(float* p, float v) { *p = v; }
 
-template <int VEC, typename OutT, typename SlotOf>
+// WPR: warps on one row (kMergeWarps / WPR rows a CTA, each its own group of warps with its
+// own named barrier, so one group may leave early without the other).
+template <int VEC, int WPR, typename OutT, typename SlotOf>
 __device__ void merge_row_chunk(const float* __restrict__ po, const float* __restrict__ pl,
                                 int count, SlotOf slot_of, int64_t r, int64_t R, int chunk,
                                 OutT* __restrict__ out_row, float* lse_out) {
   constexpr int W = 32 * VEC;                             // dv per CTA
   constexpr int NB = VEC >= 16 ? 2 : (VEC >= 4 ? 8 : 24);  // pieces per batch and warp
   constexpr int kLse = 8;                                 // lse values per lane (256 pieces)
+  constexpr int kGroupThreads = 32 * WPR;
   __shared__ __align__(16) float s_acc[kMergeWarps][W];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, gw = threadIdx.x >> 5;
+  const int g = gw / WPR, warp = gw % WPR;  // row group, warp within it
+  const int gt = threadIdx.x - g * kGroupThreads;
   if (count <= 0) {  // nothing to merge: out = 0, lse = -inf
-    for (int x = threadIdx.x; x < W; x += kMergeThreads) store_val(out_row + chunk * W + x, 0.f);
-    if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
+    for (int x = gt; x < W; x += kGroupThreads) store_val(out_row + chunk * W + x, 0.f);
+    if (gt == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
     return;
   }
   // load the pieces i0 + k * 8 (k < NB) of this warp: weights' lse values and data;
@@ -55,7 +61,7 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
   auto load_batch = [&](int i0) {
     int64_t at[NB];
 #pragma unroll
-    for (int k = 0; k < NB; ++k) at[k] = slot_of(min(i0 + k * kMergeWarps, count - 1)) * R + r;
+    for (int k = 0; k < NB; ++k) at[k] = slot_of(min(i0 + k * WPR, count - 1)) * R + r;
 #pragma unroll
     for (int k = 0; k < NB; ++k) {
       w[k] = __ldg(pl + at[k]);
@@ -76,7 +82,7 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
     }
 #pragma unroll
     for (int k = 0; k < NB; ++k)
-      if (i0 + k * kMergeWarps >= count) w[k] = -INFINITY;
+      if (i0 + k * WPR >= count) w[k] = -INFINITY;
   };
   // round one: this lane's share of the lse values, and the warp's first batch
   float lv[kLse];
@@ -127,22 +133,23 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[e] += wk * v[k][e];
       }
-      i0 += NB * kMergeWarps;
+      i0 += NB * WPR;
       if (i0 >= count) break;
       load_batch(i0);
     }
   }
 #pragma unroll
-  for (int e = 0; e < VEC; ++e) s_acc[warp][lane * VEC + e] = acc[e];
-  __syncthreads();
-  // every thread finishes W / kMergeThreads (or one) of the chunk's outputs
-  for (int x = threadIdx.x; x < W; x += kMergeThreads) {
+  for (int e = 0; e < VEC; ++e) s_acc[gw][lane * VEC + e] = acc[e];
+  // the row group's warps meet (barrier 1 + g, its threads only)
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(kGroupThreads) : "memory");
+  // every thread finishes W / kGroupThreads (or one) of the chunk's outputs
+  for (int x = gt; x < W; x += kGroupThreads) {
     float t = 0.f;
 #pragma unroll
-    for (int g = 0; g < kMergeWarps; ++g) t += s_acc[g][x];
+    for (int k = 0; k < WPR; ++k) t += s_acc[g * WPR + k][x];
     store_val(out_row + chunk * W + x, t);
   }
-  if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = lse;
+  if (gt == 0 && chunk == 0 && lse_out) *lse_out = lse;
 }
 
 // Rows of the decode/verify path whose sequence was split over several CTAs, and rows of
@@ -150,11 +157,14 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
 // of the attention kernel, whose grid it waits for; a following attention call launched
 // the same way may be scheduled from here on (its prologue overlaps this kernel, its inputs
 // are read only after this grid has completed).
-template <int VEC, typename OutT>
+template <int VEC, int WPR, typename OutT>
 __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int64_t row = blockIdx.x;  // b * R + r
+  constexpr int kRowsPerCta = kMergeWarps / WPR;
+  const int g = (threadIdx.x >> 5) / WPR, gt = threadIdx.x - g * 32 * WPR;
+  const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + g;  // b * R + r
+  if (row >= (int64_t)p.B * p.R) return;
   const int chunk = blockIdx.y;
   const int b = (int)(row / p.R);
   const int64_t r = row % p.R;
@@ -167,9 +177,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p
     out_row = p.out + row * kDV;
   float* lse_out = p.lse ? p.lse + row : nullptr;
   if (sp.num_blocks == 0) {
-    for (int x = threadIdx.x; x < 32 * VEC; x += kMergeThreads)
-      store_val(out_row + chunk * 32 * VEC + x, 0.f);
-    if (threadIdx.x == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
+    for (int x = gt; x < 32 * VEC; x += 32 * WPR) store_val(out_row + chunk * 32 * VEC + x, 0.f);
+    if (gt == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
     return;
   }
   const int64_t pre = sp.first_block;
@@ -186,7 +195,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p
     if (i == 0) return 2 * c0 + first_odd;
     return 2 * ((total >= n) ? c0 + i : range_of(pre + i, total, n));
   };
-  merge_row_chunk<VEC, OutT>(p.part_out, p.part_lse, count, slot_of, r, p.R, chunk, out_row, lse_out);
+  merge_row_chunk<VEC, WPR, OutT>(p.part_out, p.part_lse, count, slot_of, r, p.R, chunk, out_row,
+                                  lse_out);
 }
 
 template <int VEC>
@@ -194,8 +204,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     merge_standalone_kernel(const float* po, const float* pl, int S, int64_t R, uint16_t* out,
                             float* lse) {
   const int64_t row = blockIdx.x;
-  merge_row_chunk<VEC, uint16_t>(po, pl, S, [](int i) -> int64_t { return i; }, row, R, blockIdx.y,
-                                 out + row * kDV, lse ? lse + row : nullptr);
+  merge_row_chunk<VEC, kMergeWarps, uint16_t>(po, pl, S, [](int i) -> int64_t { return i; }, row, R,
+                                              blockIdx.y, out + row * kDV, lse ? lse + row : nullptr);
 }
 
 // Chunk width: whole 512-wide rows when there are rows enough to fill the GPU, narrower
@@ -211,8 +221,13 @@ int merge_vec(int64_t rows, int num_sms) {
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
   const int64_t rows = (int64_t)p.B * p.R;
   const int vec = merge_vec(rows, p.num_ctas);
+  // Whole 512-wide rows split over few CTAs each (a batch of short sequences): two rows a
+  // CTA, four warps a row (half the CTAs to launch: measured faster). Rows with many pieces
+  // (a sequence over more than 8 CTAs) keep eight warps, which load twice the pieces a round.
+  const bool two_rows = vec == 16 && p.num_ctas <= 8 * p.B;
+  const int64_t per = two_rows ? 2 : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)rows, kDV / (32 * vec));
+  cfg.gridDim = dim3((unsigned)((rows + per - 1) / per), kDV / (32 * vec));
   cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr;
@@ -221,13 +236,15 @@ cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   if (p.out_f32) {
-    if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, float>, p);
-    if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4, float>, p);
-    return cudaLaunchKernelEx(&cfg, merge_split_kernel<1, float>, p);
+    if (two_rows) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, 4, float>, p);
+    if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, kMergeWarps, float>, p);
+    if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4, kMergeWarps, float>, p);
+    return cudaLaunchKernelEx(&cfg, merge_split_kernel<1, kMergeWarps, float>, p);
   }
-  if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, uint16_t>, p);
-  if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4, uint16_t>, p);
-  return cudaLaunchKernelEx(&cfg, merge_split_kernel<1, uint16_t>, p);
+  if (two_rows) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, 4, uint16_t>, p);
+  if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, kMergeWarps, uint16_t>, p);
+  if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4, kMergeWarps, uint16_t>, p);
+  return cudaLaunchKernelEx(&cfg, merge_split_kernel<1, kMergeWarps, uint16_t>, p);
 }
 
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
