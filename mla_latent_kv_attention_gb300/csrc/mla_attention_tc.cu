@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // both are on the path to the first scores.
     if (warp >= 2 && ms->plan_b0 < B) {
       const int b0 = ms->plan_b0;
-      const int t = threadIdx.x - 64;  // 320 threads or more
+      const int t = threadIdx.x - 64;
       const int qlines = args.rows * 9;  // 1,152 bytes per row
       if (t < qlines)
         prefetch_l2(reinterpret_cast<const uint8_t*>(
@@ -601,10 +601,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       if (t < qlines && has_unit<PF>(args, ms, c1))
         prefetch_l2(reinterpret_cast<const uint8_t*>(
                         p.q + ((int64_t)c1.b * p.R + ms->row_off[t / 9]) * kD) + (t % 9) * 128);
+      // four lines of 32 page-table entries, by the CTA's last four threads (past the
+      // query lines: at most 48 rows x 9)
       const int64_t pg0 = max(0ll, ms->plan_x0 - ms->plan_pre0) * kKeyBlock / p.page_size;
-      const int64_t pg = pg0 + (int64_t)(t - 304) * 32;  // four lines of 32 entries
-      if (t >= 304 && t < 304 + 4 && pg < p.pt_stride)
-        prefetch_l2(p.page_table + (int64_t)b0 * p.pt_stride + pg);
+      const int tp = (int)threadIdx.x - (C::kThreads - 4);
+      const int64_t pg = pg0 + (int64_t)tp * 32;
+      if (tp >= 0 && pg < p.pt_stride) prefetch_l2(p.page_table + (int64_t)b0 * p.pt_stride + pg);
     }
     __syncthreads();
   }
