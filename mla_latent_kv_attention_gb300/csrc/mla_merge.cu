@@ -152,49 +152,112 @@ __device__ void merge_row_chunk(const float* __restrict__ po, const float* __res
   if (gt == 0 && chunk == 0 && lse_out) *lse_out = lse;
 }
 
+// Blocks of sequence b on the split plan's cost axis: its length clamped to what its
+// page-table row can address, as the attention kernel plans it (which also reports a
+// length out of range).
+__device__ __forceinline__ int plan_blocks(const AttnParams& p, int b) {
+  int L = __ldg(p.seq_lens + b);
+  const int64_t cap = p.pt_stride * (int64_t)p.page_size;
+  if (L < 0) L = 0;
+  if ((int64_t)L > cap) L = (int)cap;
+  return (L + kKeyBlock - 1) / kKeyBlock;
+}
+
 // Rows of the decode/verify path whose sequence was split over several CTAs, and rows of
 // sequences with no key at all (out = 0, lse = -inf). Launched as a programmatic dependent
-// of the attention kernel, whose grid it waits for; a following attention call launched
-// the same way may be scheduled from here on (its prologue overlaps this kernel, its inputs
-// are read only after this grid has completed).
+// of the attention kernel. Before waiting for that grid it works out, from the lengths
+// alone, where each of its rows' pieces sit: the lengths are inputs of the call, complete
+// before the attention kernel passed its own wait on the kernels before it, and only then
+// could this grid start. So after the wait the partials are loaded at once, and rows with
+// nothing to merge never wait. A following attention call launched the same way may be
+// scheduled from the wait on (its prologue overlaps this kernel, its inputs are read only
+// after this grid has completed).
+// Minimum resident CTAs an SM (register budget) of each instantiation, measured: two rows
+// a CTA want their registers (fewer, with spills, ran slower), one row with eight warps
+// wants three CTAs an SM (384 CTAs for 384 rows), the narrow chunks of a few long rows run
+// best with the compiler's own choice (0).
+template <int VEC, int WPR>
+constexpr int kMergeMinBlocks = (VEC == 16 && WPR == 4) ? 2 : ((VEC == 1) ? 0 : 3);
+
 template <int VEC, int WPR, typename OutT>
-__global__ void __launch_bounds__(kMergeThreads) merge_split_kernel(AttnParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
+__global__ void __launch_bounds__(kMergeThreads, kMergeMinBlocks<VEC, WPR>)
+    merge_split_kernel(AttnParams p) {
   constexpr int kRowsPerCta = kMergeWarps / WPR;
-  const int g = (threadIdx.x >> 5) / WPR, gt = threadIdx.x - g * 32 * WPR;
-  const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + g;  // b * R + r
-  if (row >= (int64_t)p.B * p.R) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = warp / WPR, gt = threadIdx.x - g * 32 * WPR;
+  const int64_t rows = (int64_t)p.B * p.R;
+  const int64_t row0 = (int64_t)blockIdx.x * kRowsPerCta;
+  // the cost axis: every sequence as kUnitCost units, then its blocks (none if empty);
+  // its length, and the units before each row group's sequence
+  int bg[kRowsPerCta];
+  long long tot = 0, before[kRowsPerCta];
+#pragma unroll
+  for (int k = 0; k < kRowsPerCta; ++k) {
+    bg[k] = (int)(min(row0 + k, rows - 1) / p.R);
+    before[k] = 0;
+  }
+  for (int x = threadIdx.x; x < p.B; x += kMergeThreads) {
+    const int nb = plan_blocks(p, x);
+    const long long cost = nb > 0 ? nb + kUnitCost : 0;
+    tot += cost;
+#pragma unroll
+    for (int k = 0; k < kRowsPerCta; ++k)
+      if (x < bg[k]) before[k] += cost;
+  }
+  __shared__ long long s_red[kMergeWarps][1 + kRowsPerCta];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+#pragma unroll
+    for (int k = 0; k < kRowsPerCta; ++k) before[k] += __shfl_xor_sync(0xffffffffu, before[k], o);
+  }
+  if (lane == 0) {
+    s_red[warp][0] = tot;
+#pragma unroll
+    for (int k = 0; k < kRowsPerCta; ++k) s_red[warp][1 + k] = before[k];
+  }
+  __syncthreads();
+  long long total = 0, pre = 0;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) {
+    total += s_red[w][0];
+    pre += s_red[w][1 + g];
+  }
+  const int64_t row = row0 + g;  // b * R + r
+  if (row >= rows) return;
   const int chunk = blockIdx.y;
-  const int b = (int)(row / p.R);
+  static_assert(kRowsPerCta <= 2, "row groups a CTA");
+  const int b = (g == 0) ? bg[0] : bg[kRowsPerCta - 1];  // (no indexing of a local array)
   const int64_t r = row % p.R;
-  const SeqSpan sp = p.seqs[b];
-  const int64_t total = p.hdr->total_cost, n = p.num_ctas;
+  const int num_blocks = plan_blocks(p, b);
   OutT* out_row;
   if constexpr (sizeof(OutT) == 4)
     out_row = p.out_f32 + row * kDV;
   else
     out_row = p.out + row * kDV;
   float* lse_out = p.lse ? p.lse + row : nullptr;
-  if (sp.num_blocks == 0) {
+  if (num_blocks == 0) {  // no unit of the attention kernel touches these rows
     for (int x = gt; x < 32 * VEC; x += 32 * WPR) store_val(out_row + chunk * 32 * VEC + x, 0.f);
     if (gt == 0 && chunk == 0 && lse_out) *lse_out = -INFINITY;
     return;
   }
-  const int64_t pre = sp.first_block;
+  const int64_t n = p.num_ctas;
+  const int64_t first = pre + kUnitCost;  // the sequence's first block
   // pieces: one per CTA range the sequence's blocks overlap (with fewer blocks than CTAs
   // every range holds at most one block)
-  const int64_t c0 = range_of(pre, total, n);
-  const int count = (total >= n) ? (int)(range_of(pre + sp.num_blocks - 1, total, n) - c0 + 1)
-                                 : sp.num_blocks;
-  if (count == 1) return;  // the attention kernel wrote this row itself
+  const int64_t c0 = range_of(first, total, n);
+  const int count = (total >= n) ? (int)(range_of(first + num_blocks - 1, total, n) - c0 + 1)
+                                 : num_blocks;
+  if (count == 1) return;  // the attention kernel writes this row itself
   // piece 0 takes the second slot of its CTA when that CTA's range began before this
   // sequence's span (in an earlier sequence); every later piece begins its CTA's range
-  const int64_t first_odd = (range_lo(c0, total, n) < pre - kUnitCost) ? 1 : 0;
+  const int64_t first_odd = (range_lo(c0, total, n) < first - kUnitCost) ? 1 : 0;
   auto slot_of = [&](int i) -> int64_t {
     if (i == 0) return 2 * c0 + first_odd;
-    return 2 * ((total >= n) ? c0 + i : range_of(pre + i, total, n));
+    return 2 * ((total >= n) ? c0 + i : range_of(first + i, total, n));
   };
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   merge_row_chunk<VEC, WPR, OutT>(p.part_out, p.part_lse, count, slot_of, r, p.R, chunk, out_row,
                                   lse_out);
 }
