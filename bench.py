@@ -456,14 +456,21 @@ def secondary_workloads(dev, hbm_peak, bf16_peak, steps):
     ws = mla.workspace(mla.MLA_OP_PREFILL, 1, inp.H, inp.n_q, dev)
     out = torch.empty(inp.n_q, inp.H, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(inp.n_q, inp.H, dtype=torch.float32, device=dev)
+    # clocks while the chunk runs back to back (a tensor-bound kernel of several ms meets
+    # the power cap: which peak, burst or sustained, it is held against)
+    pf_clocks = ClockSampler(torch.cuda.current_device())
+    pf_clocks.start()
+    pf_clocks.mark("t0")
     ms = _time_events(lambda i: mla.mla_prefill(kv, q, inp.sm_scale, out=out, lse=lse, ws=ws),
                       max(3, steps // 5), 2)
+    pf_clocks.mark("t1")
     flops = accounting.attention_flops(inp.seq_lens.tolist(), inp.n_q, inp.H)
     tf = flops / (ms / 1e3) / 1e12
     res["causal_prefill"] = {"ms_per_chunk": ms, "tok_s": inp.n_q / (ms / 1e3), "TFLOP_s": tf,
                              "frac_of_bf16_peak": tf / bf16_peak,
                              "frac_of_bf16_sustained_peak": tf / sustained_bf16_peak(),
-                             "algorithmic_flops": flops, "T": inp.n_q, "prefix": 32768, "H": inp.H}
+                             "algorithmic_flops": flops, "T": inp.n_q, "prefix": 32768, "H": inp.H,
+                             "clocks": pf_clocks.stop()}
     del kv, q, out, lse, ws
     # the same chunk in the MHA form (latent up-projected per head, then causal attention):
     # the whole call (dequantise + up-projection GEMM + attention) and the attention kernel

@@ -157,6 +157,10 @@ mla_status_t mla_verify_f32_shard(const mla_kv_t* kv, const void* q, int B, int 
  *   q    device, [T][H][576] bfloat16
  *   out  device, [T][H][512] bfloat16
  *   lse  device, [T][H] float32, or NULL
+ * Blocks of 48 / H positions go to the SMs a round at a time, longest first. When the
+ * last round would leave SMs idle, its blocks run as a second kernel over their keys'
+ * two halves and a third kernel merges the halves (the workspace holds their partials):
+ * one launch or three, all on `stream`.
  */
 mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float sm_scale,
                          void* out, float* lse, void* workspace, size_t workspace_bytes,

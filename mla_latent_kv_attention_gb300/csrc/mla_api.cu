@@ -55,6 +55,7 @@ mla::AttnParams base_params(const mla_kv_t* kv, const void* q, int B, int n_q, i
   p.n_q = n_q;
   p.H = H;
   p.R = n_q * H;
+  p.part_rows = p.R;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.trace = g_trace;
@@ -274,6 +275,9 @@ mla_status_t mla_prefill(const mla_kv_t* kv, const void* q, int T, int H, float 
   p.status = reinterpret_cast<unsigned*>(base + mla::ws_prefill_status(sms));
   p.qimg = reinterpret_cast<uint8_t*>(base + mla::ws_prefill_qimg(sms));
   p.qimg_stride = (int64_t)mla::qimg_bytes(48);
+  p.part_lse = reinterpret_cast<float*>(base + mla::ws_prefill_part_lse(sms));
+  p.part_out = reinterpret_cast<float*>(base + mla::ws_prefill_part_out(sms));
+  p.part_rows = 48;
   p.num_ctas = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   prof_mark(g_prof_start, s);

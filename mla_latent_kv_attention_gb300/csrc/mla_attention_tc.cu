@@ -183,6 +183,8 @@ struct DecodeArgs {
   int prefill;    // 1: units are blocks of P new positions of one sequence (no split plan)
   int P;          // prefill: new positions per unit
   int num_units;  // prefill: ceil(n_q / P)
+  int unit_end;   // prefill: this launch's units are [blockIdx.x, unit_end) in steps of the grid
+  int split_base;  // prefill: units [split_base, num_units) run as two halves each
   int status_overwrite;  // 1: each CTA writes its status word even when clean (first launch)
 };
 
@@ -225,9 +227,11 @@ __device__ __forceinline__ void store_out(const AttnParams& p, int64_t idx, floa
     p.out[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// PF: the launch is a prefill (units are blocks of new positions; no split plan). A
-// compile-time flag: the decode kernel then carries none of the prefill paths.
-template <bool PF>
+// PF: 0 decode/verify (the split plan's units); 1 prefill (units are blocks of new
+// positions, one a round per CTA); 2 prefill, the two halves along the keys of each unit of
+// an incomplete last round (one half a CTA, a partial for the merge). A compile-time
+// parameter: each kernel carries only its own paths.
+template <int PF>
 __device__ __forceinline__ Cursor first_unit(const DecodeArgs& a, const Misc* ms) {
   Cursor c;
   c.u = blockIdx.x;
@@ -237,14 +241,14 @@ __device__ __forceinline__ Cursor first_unit(const DecodeArgs& a, const Misc* ms
   return c;
 }
 
-template <bool PF>
+template <int PF>
 __device__ __forceinline__ bool has_unit(const DecodeArgs& a, const Misc* ms, const Cursor& c) {
-  return PF ? c.u < a.num_units : (c.b < a.p.B && c.pre < ms->plan_x1);
+  return PF ? c.u < a.unit_end : (c.b < a.p.B && c.pre < ms->plan_x1);
 }
 
 // The next unit: the next sequence with at least one key (decode/verify), or the next
 // unit index this CTA owns (prefill).
-template <bool PF>
+template <int PF>
 __device__ __forceinline__ Cursor next_unit(const DecodeArgs& a, Cursor c) {
   if (PF) {
     c.u += gridDim.x;
@@ -259,7 +263,7 @@ __device__ __forceinline__ Cursor next_unit(const DecodeArgs& a, Cursor c) {
   return c;
 }
 
-template <bool PF>
+template <int PF>
 __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, const Misc* ms, const Cursor& c) {
   const AttnParams& p = a.p;
   UnitInfo x;
@@ -278,7 +282,9 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, const Misc* m
     x.slot = 2 * (int)blockIdx.x + (c.pre - kUnitCost <= ms->plan_x0 ? 0 : 1);
   } else {
     // the last positions see the most keys: hand those out first
-    const int pos0 = (a.num_units - 1 - c.u) * a.P;
+    int v = c.u;
+    if constexpr (PF == 2) v = a.split_base + c.u / 2;  // unit v, half c.u & 1
+    const int pos0 = (a.num_units - 1 - v) * a.P;
     const int npos = min(a.P, p.n_q - pos0);
     const int L = seq_len_of(p, 0);
     x.b = 0;
@@ -290,6 +296,15 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, const Misc* m
     x.rows = npos * p.H;
     x.final_out = 1;
     x.slot = 0;
+    if constexpr (PF == 2) {  // keys [0, mid) or [mid, key_hi), partial slot c.u
+      const int mid = min(x.key_hi, ((x.key_hi + 2 * kTileKeys - 1) / (2 * kTileKeys)) * kTileKeys);
+      if (c.u & 1)
+        x.key_lo = mid;
+      else
+        x.key_hi = mid;
+      x.final_out = 0;
+      x.slot = c.u;
+    }
   }
   return x;
 }
@@ -459,7 +474,7 @@ __device__ __forceinline__ void stage_rows(const AttnParams& p, int R, const int
   }
 }
 
-template <int RP, bool PF, bool TR>
+template <int RP, int PF, bool TR>
 __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ DecodeArgs args,
                      const __grid_constant__ CUtensorMap map_main,
@@ -947,7 +962,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             for (int dv = i; dv < kDV; dv += 128) store_out(p, row * kDV + dv, 0.f);
             if (i == 0 && p.lse) p.lse[row] = -INFINITY;
           } else if (i == 0) {
-            p.part_lse[(int64_t)un.slot * p.R + ms->row_off[r]] = -INFINITY;
+            p.part_lse[(int64_t)un.slot * p.part_rows + ms->row_off[r]] = -INFINITY;
           }
         }
         continue;
@@ -1201,7 +1216,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             if (final_out) {
               store_out(p, ((int64_t)un.qrow0 + roffs[e]) * kDV + dv, acc * inv[r]);
             } else {
-              p.part_out[((int64_t)un.slot * p.R + roffs[e]) * kDV + dv] = acc * inv[r];
+              p.part_out[((int64_t)un.slot * p.part_rows + roffs[e]) * kDV + dv] = acc * inv[r];
             }
           }
         }
@@ -1220,7 +1235,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         if (final_out) {
           if (p.lse) p.lse[(int64_t)un.qrow0 + roff] = lse;
         } else {
-          p.part_lse[(int64_t)un.slot * p.R + roff] = lse;
+          p.part_lse[(int64_t)un.slot * p.part_rows + roff] = lse;
         }
       }
       ++k;
@@ -1294,7 +1309,7 @@ bool encode_pool_maps(const AttnParams& p, CUtensorMap* main_map, CUtensorMap* t
   return r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS;
 }
 
-template <int RP, bool PF, bool TR>
+template <int RP, int PF, bool TR>
 cudaError_t launch_rp_tr(const DecodeArgs& a, const CUtensorMap& mm, const CUtensorMap& mt,
                          int grid, cudaStream_t s) {
   constexpr int smem = smem_bytes<RP>();
@@ -1314,11 +1329,15 @@ cudaError_t launch_rp_tr(const DecodeArgs& a, const CUtensorMap& mm, const CUten
   return cudaLaunchKernelEx(&cfg, attn_tc_kernel<RP, PF, TR>, a, mm, mt);
 }
 
-template <int RP, bool PF>
+template <int RP, int PF>
 cudaError_t launch_rp(const DecodeArgs& a, const CUtensorMap& mm, const CUtensorMap& mt,
                       int grid, cudaStream_t s) {
-  return a.p.trace ? launch_rp_tr<RP, PF, true>(a, mm, mt, grid, s)
-                   : launch_rp_tr<RP, PF, false>(a, mm, mt, grid, s);
+  if constexpr (PF == 2) {  // (never traced)
+    return launch_rp_tr<RP, PF, false>(a, mm, mt, grid, s);
+  } else {
+    return a.p.trace ? launch_rp_tr<RP, PF, true>(a, mm, mt, grid, s)
+                     : launch_rp_tr<RP, PF, false>(a, mm, mt, grid, s);
+  }
 }
 
 }  // namespace
@@ -1341,14 +1360,16 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
     a.prefill = 0;
     a.P = 0;
     a.num_units = 0;
+    a.unit_end = 0;
+    a.split_base = 0;
     a.status_overwrite = (gi == 0);
     cudaError_t e;
     if (a.rows <= 16)
-      e = launch_rp<16, false>(a, mm, mt, grid, s);
+      e = launch_rp<16, 0>(a, mm, mt, grid, s);
     else if (a.rows <= 32)
-      e = launch_rp<32, false>(a, mm, mt, grid, s);
+      e = launch_rp<32, 0>(a, mm, mt, grid, s);
     else
-      e = launch_rp<48, false>(a, mm, mt, grid, s);
+      e = launch_rp<48, 0>(a, mm, mt, grid, s);
     if (e != cudaSuccess) return e;
     ++*launches;
   }
@@ -1356,8 +1377,9 @@ cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, i
 }
 
 // Causal prefill of one sequence: units are blocks of P = 48 / H new positions (all their
-// heads, at most 48 rows) over every key they see, handed out longest first. No split of
-// the key axis (there are thousands of units), so no split plan and no merge.
+// heads, at most 48 rows) over every key they see, handed out longest first, one a round
+// per CTA. A last round that would leave CTAs idle runs instead as a second launch over
+// the halves of its units (keys split in two), and a merge kernel joins the halves.
 cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches) {
   CUtensorMap mm, mt;
   if (!encode_pool_maps(p, &mm, &mt)) return cudaErrorInvalidValue;
@@ -1371,9 +1393,23 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, 
   a.status_overwrite = 1;
   a.num_units = (p.n_q + a.P - 1) / a.P;
   const int grid = min(num_sms, a.num_units);
-  const cudaError_t e = launch_rp<48, true>(a, mm, mt, grid, s);
-  if (e == cudaSuccess) ++*launches;
-  return e;
+  const int left = a.num_units % grid;  // units of an incomplete last round
+  const bool split = left > 0 && 2 * left <= grid;
+  a.split_base = a.num_units - left;
+  a.unit_end = split ? a.split_base : a.num_units;
+  cudaError_t e = launch_rp<48, 1>(a, mm, mt, grid, s);
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  if (!split) return cudaSuccess;
+  DecodeArgs b = a;
+  b.unit_end = 2 * left;  // halves: one a CTA
+  b.status_overwrite = 0;
+  b.p.trace = nullptr;    // the profiling hook traces the main launch
+  if ((e = launch_rp<48, 2>(b, mm, mt, 2 * left, s)) != cudaSuccess) return e;
+  ++*launches;
+  if ((e = launch_merge_prefill(p, a.P, left, s)) != cudaSuccess) return e;
+  ++*launches;
+  return cudaSuccess;
 }
 
 }  // namespace mla

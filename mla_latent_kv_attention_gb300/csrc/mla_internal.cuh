@@ -79,13 +79,21 @@ inline WsLayout ws_layout(int B, int rows_per_seq, int num_sms) {
   return w;
 }
 
-// Prefill: the header, the per-CTA status words and the per-CTA query images (48 rows).
+// Prefill: the header, the per-CTA status words, the per-CTA query images (48 rows), and
+// the partials of the units of the last round that are split in two along the keys: one
+// slot per CTA, 48 rows each (float32 LSE, then float32 outputs).
 inline size_t ws_prefill_status(int) { return align_up(sizeof(WsHeader), 256); }
 inline size_t ws_prefill_qimg(int num_sms) {
   return align_up(ws_prefill_status(num_sms) + sizeof(unsigned) * (size_t)num_sms, 256);
 }
+inline size_t ws_prefill_part_lse(int num_sms) {
+  return align_up(ws_prefill_qimg(num_sms) + qimg_bytes(48) * (size_t)num_sms, 256);
+}
+inline size_t ws_prefill_part_out(int num_sms) {
+  return align_up(ws_prefill_part_lse(num_sms) + sizeof(float) * 48 * (size_t)num_sms, 256);
+}
 inline size_t ws_prefill_bytes(int num_sms) {
-  return ws_prefill_qimg(num_sms) + qimg_bytes(48) * (size_t)num_sms;
+  return align_up(ws_prefill_part_out(num_sms) + sizeof(float) * 48 * kDV * (size_t)num_sms, 256);
 }
 
 // Everything an attention kernel needs for one call.
@@ -103,8 +111,9 @@ struct AttnParams {
   uint16_t* out;      // [B][n_q][H][512] bf16
   float* out_f32;     // when set, the output goes here as float32 instead of to `out`
   float* lse;         // [B][n_q][H] or null
-  float* part_out;    // [2 * num_ctas][R][512]
-  float* part_lse;    // [2 * num_ctas][R]
+  float* part_out;    // [slots][part_rows][512]
+  float* part_lse;    // [slots][part_rows]
+  int part_rows;      // rows of a partial slot: R (decode/verify), 48 (prefill)
   SeqSpan* seqs;      // [B]
   unsigned* status;   // [num_ctas]
   uint8_t* qimg;      // [num_ctas] staged query images, qimg_stride bytes apart
@@ -198,6 +207,7 @@ struct MhaArgs {
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_decode_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_prefill_tc(const AttnParams& p, int num_sms, cudaStream_t s, int* launches);
+cudaError_t launch_merge_prefill(const AttnParams& p, int P, int split_units, cudaStream_t s);
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,
                                     uint16_t* out, float* lse, int num_sms, cudaStream_t s);
 cudaError_t launch_cache_append(uint8_t* pool, int64_t pool_rows, const uint16_t* x,

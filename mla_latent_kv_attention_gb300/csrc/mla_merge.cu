@@ -262,6 +262,34 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeMinBlocks<VEC, WPR>)
                                   lse_out);
 }
 
+// Prefill units of an incomplete last round, each run as two halves along the keys: split
+// unit v (v = 0 .. split_units - 1, the units handed out last, i.e. the first positions)
+// covers positions [pos0, pos0 + npos) with rows j * H + h, and its halves sit in partial
+// slots 2v and 2v + 1 of 48 rows. Two rows a CTA (four warps a row), 24 CTAs a unit.
+template <typename OutT>
+__global__ void __launch_bounds__(kMergeThreads, 2)
+    merge_prefill_kernel(AttnParams p, int P, int split_units) {
+  constexpr int WPR = 4;
+  const int g = (threadIdx.x >> 5) / WPR;
+  const int v = blockIdx.x / 24;
+  const int r = (blockIdx.x % 24) * 2 + g;  // row of the unit
+  const int pos0 = (split_units - 1 - v) * P;
+  const int npos = min(P, p.n_q - pos0);
+  if (r >= npos * p.H) return;
+  const int64_t row = (int64_t)pos0 * p.H + r;
+  OutT* out_row;
+  if constexpr (sizeof(OutT) == 4)
+    out_row = p.out_f32 + row * kDV;
+  else
+    out_row = p.out + row * kDV;
+  float* lse_out = p.lse ? p.lse + row : nullptr;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  merge_row_chunk<16, WPR, OutT>(p.part_out, p.part_lse, 2,
+                                 [v](int i) -> int64_t { return 2 * v + i; }, r, p.part_rows, 0,
+                                 out_row, lse_out);
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_standalone_kernel(const float* po, const float* pl, int S, int64_t R, uint16_t* out,
@@ -308,6 +336,21 @@ cudaError_t launch_merge(const AttnParams& p, cudaStream_t s) {
   if (vec == 16) return cudaLaunchKernelEx(&cfg, merge_split_kernel<16, kMergeWarps, uint16_t>, p);
   if (vec == 4) return cudaLaunchKernelEx(&cfg, merge_split_kernel<4, kMergeWarps, uint16_t>, p);
   return cudaLaunchKernelEx(&cfg, merge_split_kernel<1, kMergeWarps, uint16_t>, p);
+}
+
+cudaError_t launch_merge_prefill(const AttnParams& p, int P, int split_units, cudaStream_t s) {
+  if (split_units <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)split_units * 24);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (p.out_f32) return cudaLaunchKernelEx(&cfg, merge_prefill_kernel<float>, p, P, split_units);
+  return cudaLaunchKernelEx(&cfg, merge_prefill_kernel<uint16_t>, p, P, split_units);
 }
 
 cudaError_t launch_merge_standalone(const float* part_out, const float* part_lse, int S, int64_t R,

@@ -136,6 +136,22 @@ def test_causal_prefill_small(T, prefix, H):
     compare(out, lse, ref_out, ref_lse, f"prefill T={T} prefix={prefix}")
 
 
+@pytest.mark.parametrize("prefix,H", [(0, 12), (2000, 12), (500, 8)])
+def test_causal_prefill_split_last_round(prefix, H):
+    """Position blocks one and a quarter times the SM count: the blocks of the incomplete
+    last round (the first positions) run as two halves along the keys on different CTAs
+    and are merged. With no prefix the first blocks see fewer than 128 keys, so their
+    second half is empty (a partial with lse = -inf)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    P = 48 // H
+    units = sms + sms // 4
+    T = units * P - 1  # the last position block (handed out first) is ragged
+    inp = W.causal_prefill(T=T, prefix=prefix, H=H, seed=7 + prefix + H)
+    out, lse = run_prefill(inp)
+    ref_out, ref_lse = oracle.attention(inp)
+    compare(out, lse, ref_out, ref_lse, f"prefill T={T} prefix={prefix} H={H} (split last round)")
+
+
 def test_causal_prefill_full_sampled():
     """8,192 new positions on a 32,768-position prefix, 12 heads: every row is computed on
     the GPU; the oracle checks every head of the first six positions (the first sits on
