@@ -287,6 +287,12 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   auto tail_key = [&](int64_t q) -> unsigned {
     return q < span ? (__float_as_uint(__ldcs(p + (q - off))) & 0x7FFFFFFFu) : 0u;
   };
+  // outputs: whole 16-byte vectors where the output row has the input's alignment and all
+  // four positions are in the row, single entries elsewhere
+  const uintptr_t oa = reinterpret_cast<uintptr_t>(o);
+  const bool vec_out = (int)((oa & 15u) >> 2) == off;
+  float4* o4 = reinterpret_cast<float4*>(oa - (oa & 15u));
+  unsigned written = 0;  // bit j: vector j of this thread was stored early (all zeros)
   const int kk = top_k ? top_k[row] : k_all;
   unsigned pivot = 0;     // lowest kept bit pattern; 0 keeps everything
   bool have_inv = false;  // the candidate path delivered 1 / (kept sum) with the pivot
@@ -350,6 +356,20 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     select_bin(s, s.sel, k - above_sl, kSliceBins);
     unsigned prefix = (unsigned)(S * kSliceBins + s.bin);  // the sign bit (0), then bits 30..20
     k -= above_sl + s.above;
+    // Every entry below the selected bin is cut, whatever the rest of the selection finds:
+    // whole vectors of such entries are stored (as zeros) now, while the cluster finishes
+    // the selection, rather than all at the end.
+    if (vec_out) {
+#pragma unroll
+      for (int j = 0; j < kTkVec; ++j) {
+        const int64_t v = v0 + (int64_t)j * kTkThreads, q0 = 4 * v;
+        const unsigned hi = max(max(key[4 * j], key[4 * j + 1]), max(key[4 * j + 2], key[4 * j + 3]));
+        if (q0 >= off && q0 + 3 < span && (hi >> 20) < prefix) {
+          __stcs(o4 + v, make_float4(0.f, 0.f, 0.f, 0.f));
+          written |= 1u << j;
+        }
+      }
+    }
     int done = 12;
     if (k == s.in_bin) {
       // the bin is kept whole: its lowest pattern is the pivot
@@ -431,15 +451,10 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     }
     inv = 1.f / total;
   }
-  // outputs: whole 16-byte vectors where the output row has the input's alignment and all
-  // four positions are in the row, single entries elsewhere
-  const uintptr_t oa = reinterpret_cast<uintptr_t>(o);
-  const bool vec_out = (int)((oa & 15u) >> 2) == off;
-  float4* o4 = reinterpret_cast<float4*>(oa - (oa & 15u));
 #pragma unroll
   for (int j = 0; j < kTkVec; ++j) {
     const int64_t v = v0 + (int64_t)j * kTkThreads, q0 = 4 * v;
-    if (q0 >= span) continue;
+    if (q0 >= span || ((written >> j) & 1u)) continue;
     float r4[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
