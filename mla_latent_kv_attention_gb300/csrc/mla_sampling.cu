@@ -17,10 +17,11 @@
 // of the entries still in play, counted by every CTA into its own shared memory. Selection
 // stops early when the bin that holds the k-th largest entry is kept whole.
 //
-// First pass: the 2,048 bins are cut into eight slices of 256; each CTA adds up its slices
-// over the cluster (distributed shared memory), the CTAs read the eight slice totals, and
-// each fetches the one slice that holds the k-th largest entry to select the bin in it:
-// about 9 KB of remote reads a CTA where every CTA gathering every histogram took 64 KB.
+// First pass: the 2,048 bins are cut into eight slices of 256. Before the cluster barrier
+// each CTA counts its entries per slice; after it every CTA reads the n CTAs' eight slice
+// counts, finds the slice that holds the k-th largest entry and adds up that slice's bins
+// over the cluster (distributed shared memory) to select the bin in it: about 8 KB of
+// remote reads a CTA and one barrier, where every CTA gathering every histogram took 64 KB.
 //
 // The selected bin usually holds a few dozen entries of the row. When it holds at most
 // kCandCap, the cluster skips the remaining passes: every CTA sends the bin's entries (their
@@ -55,11 +56,11 @@ __device__ constexpr int digit_width(int pass) { return pass == kPasses - 1 ? 9 
 
 struct __align__(16) TkSmem {
   unsigned hist[kPasses][kBins];  // this CTA's counts, one buffer a pass (read remotely)
-  unsigned tot[kBins];            // the cluster's counts: this CTA's first-pass slices (read
-                                  // remotely), or every bin of a later pass
-  unsigned sel[kSliceBins];       // first pass: the slice that holds the k-th largest entry
-  unsigned slice_tot[kSlices];    // totals of the first-pass slices this CTA adds up
-  unsigned slice_all[kSlices];    // totals of all eight
+  unsigned tot[kBins];            // the cluster's counts of every bin of a later pass (rank 0:
+                                  // its local passes over the candidates)
+  unsigned sel[kSliceBins];       // first pass: the cluster's counts of the selected slice
+  unsigned slice_tot[kSlices];    // this CTA's first-pass count in each slice (read remotely)
+  unsigned slice_all[kSlices];    // the cluster's count of each slice
   unsigned wsum[kWarps];
   float wsum_f[kWarps];
   float part;                     // this CTA's kept sum (read by the other CTAs)
@@ -310,48 +311,50 @@ __global__ void __launch_bounds__(kTkThreads, 2)
       for (int j = 0; j < kTkPerThread; ++j) atomicAdd(&hist[key[j] >> 20], 1u);
       for (int64_t i = tail0 + lane; i < span; i += tail_step) atomicAdd(&hist[tail_key(i) >> 20], 1u);
     }
-    sm100::cluster_sync();  // every CTA's first-pass histogram is complete
+    __syncthreads();
     {
-      // this CTA adds up slices rank, rank + n, ... over the cluster: 64 threads a slice
-      const int g = t >> 6, gt = t & 63;
-      const int sl = (int)rank + g * n;
-      unsigned sum = 0;
-      if (sl < kSlices) {
-        const int b0 = sl * kSliceBins + 4 * gt;
-        uint4 c = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int r0 = 0; r0 < kTkMaxCluster; r0 += 4) {
-          uint4 v[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            if (r0 + r < n) v[r] = sm100::ld_dsmem_v4(&s.hist[0][b0], (uint32_t)(r0 + r));
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            if (r0 + r < n) {
-              c.x += v[r].x;
-              c.y += v[r].y;
-              c.z += v[r].z;
-              c.w += v[r].w;
-            }
-        }
-        *reinterpret_cast<uint4*>(&s.tot[b0]) = c;
-        sum = c.x + c.y + c.z + c.w;
-      }
-      sum = __reduce_add_sync(0xffffffffu, sum);
+      // this CTA's count in each 256-bin slice: four bins a thread, two warps a slice
+      const uint4 c = *reinterpret_cast<const uint4*>(&s.hist[0][4 * t]);
+      const unsigned sum = __reduce_add_sync(0xffffffffu, c.x + c.y + c.z + c.w);
       if (lane == 0) s.wsum[warp] = sum;
       __syncthreads();
-      if (gt == 0 && sl < kSlices) s.slice_tot[sl] = s.wsum[2 * g] + s.wsum[2 * g + 1];
+      if (t < kSlices) s.slice_tot[t] = s.wsum[2 * t] + s.wsum[2 * t + 1];
     }
-    sm100::cluster_sync();  // every slice added up, every slice total written
-    if (t < kSlices) s.slice_all[t] = sm100::ld_dsmem_u32(&s.slice_tot[t], (uint32_t)(t % n));
+    sm100::cluster_sync();  // every CTA's first-pass histogram and slice counts are complete
+    // the cluster's count of each slice: eight threads, every CTA's count in one round
+    if (t < kSlices) {
+      unsigned v[kTkMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kTkMaxCluster; ++r)
+        v[r] = r < n ? sm100::ld_dsmem_u32(&s.slice_tot[t], (uint32_t)r) : 0u;
+      unsigned a = 0;
+#pragma unroll
+      for (int r = 0; r < kTkMaxCluster; ++r) a += v[r];
+      s.slice_all[t] = a;
+    }
     __syncthreads();
-    // the slice that holds the k-th largest entry (slices from the top), then its bins
+    // the slice that holds the k-th largest entry (slices from the top), then its 256 bins
+    // added up over the cluster (64 threads, four bins each, every CTA's counts in one round)
     int S = kSlices - 1;
     unsigned above_sl = 0;
     while (S > 0 && above_sl + s.slice_all[S] < k) above_sl += s.slice_all[S--];
-    if (t < kSliceBins / 4)
-      *reinterpret_cast<uint4*>(&s.sel[4 * t]) =
-          sm100::ld_dsmem_v4(&s.tot[S * kSliceBins + 4 * t], (uint32_t)(S % n));
+    if (t < kSliceBins / 4) {
+      const int b0 = S * kSliceBins + 4 * t;
+      uint4 v[kTkMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kTkMaxCluster; ++r)
+        if (r < n) v[r] = sm100::ld_dsmem_v4(&s.hist[0][b0], (uint32_t)r);
+      uint4 c = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int r = 0; r < kTkMaxCluster; ++r)
+        if (r < n) {
+          c.x += v[r].x;
+          c.y += v[r].y;
+          c.z += v[r].z;
+          c.w += v[r].w;
+        }
+      *reinterpret_cast<uint4*>(&s.sel[4 * t]) = c;
+    }
     __syncthreads();
     select_bin(s, s.sel, k - above_sl, kSliceBins);
     unsigned prefix = (unsigned)(S * kSliceBins + s.bin);  // the sign bit (0), then bits 30..20
