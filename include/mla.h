@@ -84,8 +84,8 @@ typedef struct mla_kv {
 
 /*
  * Bytes of workspace the given call needs on `device` (a CUDA ordinal). The workspace
- * holds each sequence's place in the split plan, the per-split partial outputs and one
- * status word per CTA; it must be 256-byte aligned and stay untouched until the call's
+ * holds the per-split partial outputs, staged query rows and one status word per CTA (it
+ * depends on H, n_q and the SM count, not on B); it must be 256-byte aligned and stay untouched until the call's
  * work has finished on its stream. Its contents need no initialisation: every call
  * rewrites all it later reads (zero-fill it once if mla_read_status may run before the
  * first call). For MLA_OP_PREFILL pass B = 1 and n_q = T. Returns 0 for unsupported
@@ -292,11 +292,13 @@ void mla_set_profile_events(void* start, void* stop);
  * Profiling hook. With a device buffer of `bytes` (8-byte aligned), the next decode /
  * verify / prefill calls on this host thread make each CTA c of their attention kernel
  * (while c < bytes / 128) write sixteen 64-bit words at buffer + 128 c: the GPU's global
- * timer (ns) at entry, after the wait on the previous kernel, after the split plan, when
- * the first tile's scores were read, when the last tile's probabilities were written, when
- * the last values MMA completed, after its last epilogue and at exit; then (tiles << 32 |
- * units) it processed; then, for CTAs with two units or more, the end of the first unit's
- * epilogue and the second unit's first scores (words 11-15 are not written). NULL switches
+ * timer (ns) at entry, after the wait on the previous kernel, after the split plan and the
+ * first tile loads issued, when the first tile's scores were read, when the last tile's
+ * probabilities were written, when the last values MMA completed, after its last epilogue
+ * and at exit; then (tiles << 32 | units) it processed; then, for CTAs with two units or
+ * more, the end of the first unit's epilogue and the second unit's first scores; then
+ * (decode / verify) the end of the plan's scan and the end of its L2 prefetches (words 13-15
+ * are not written). NULL switches
  * it off. The buffer stays owned by the caller; the results are undefined while two calls
  * overlap on the GPU.
  */
@@ -312,11 +314,11 @@ void mla_set_trace_buffer(void* device_buffer, size_t bytes);
  * of MLA_STATIC_WS_BYTES owned by the library in device memory: every GPU on which the
  * library's kernels are loaded holds it until the process exits. No memory is allocated
  * by this call.
- *  - A batch whose mla_workspace_size(MLA_OP_DECODE, B, H, 1, device) exceeds
- *    MLA_STATIC_WS_BYTES is rejected with MLA_ERR_WORKSPACE before anything is enqueued
- *    (16 MiB covers 16-head decode of any batch up to several hundred thousand
- *    sequences on a 152-SM GB300: the partial outputs and staged query rows take about
- *    13 MB of it).
+ *  - A call whose mla_workspace_size(MLA_OP_DECODE, B, H, 1, device) exceeds
+ *    MLA_STATIC_WS_BYTES is rejected with MLA_ERR_WORKSPACE before anything is enqueued.
+ *    The decode workspace grows with H and the SM count, not with B: 16 MiB covers
+ *    16-head decode of any batch on a 152-SM GB300 (the partial outputs and staged query
+ *    rows take about 13 MB of it).
  *  - The first call on each device (and the first after the device's context changed,
  *    for instance after cudaDeviceReset) looks up the array's device address (a runtime
  *    symbol query); make that first call outside any CUDA stream capture.

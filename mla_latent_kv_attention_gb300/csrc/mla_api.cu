@@ -104,7 +104,6 @@ mla_status_t run_split(const mla_kv_t* kv, const void* q, int B, int n_q, int H,
   char* base = static_cast<char*>(ws);
   p.hdr = reinterpret_cast<mla::WsHeader*>(base + w.hdr);
   p.status = reinterpret_cast<unsigned*>(base + w.status);
-  p.seqs = reinterpret_cast<mla::SeqSpan*>(base + w.seqs);
   p.part_lse = reinterpret_cast<float*>(base + w.part_lse);
   p.part_out = reinterpret_cast<float*>(base + w.part_out);
   p.qimg = reinterpret_cast<uint8_t*>(base + w.qimg);

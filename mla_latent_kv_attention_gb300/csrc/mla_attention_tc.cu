@@ -592,15 +592,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         ms->plan_pre0 = first;
         ms->plan_L0 = seq_len_of(p, b);
       }
-      if (b % (int)n == (int)c) p.seqs[b] = SeqSpan{(int)first, nb};
       if (nb > 0) pre = first + nb;
     }
     if (tid == 0) {
       ms->plan_x0 = x0;
       ms->plan_x1 = x1;
-      if (c == 0) p.hdr->total_cost = (int)total;
     }
     __syncthreads();
+    if (trace && threadIdx.x == 0) trace[kTrPlanScan] = globaltimer_ns();
     // Ask L2 for the first unit's query rows and page-table entries before the first TMA
     // loads go out: behind the initial burst of key traffic they would arrive late, and
     // both are on the path to the first scores.
@@ -624,6 +623,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
       if (tp >= 0 && pg < p.pt_stride) prefetch_l2(p.page_table + (int64_t)b0 * p.pt_stride + pg);
     }
     __syncthreads();
+    if (trace && threadIdx.x == 0) trace[kTrPlanPrefetch] = globaltimer_ns();
   }
   // Loads of one key tile into its stage (producer thread): the two 64-key halves' pool rows
   // from the page table, then the stage's two halves, each once the MMAs of the tile that

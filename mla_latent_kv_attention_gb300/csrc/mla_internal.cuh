@@ -20,16 +20,7 @@ constexpr int kMaxRows = MLA_MAX_HEADS * MLA_MAX_NQ;  // query rows per sequence
 // Workspace header at offset 0 (256 bytes).
 struct WsHeader {
   int num_ctas;      // CTAs of the last attention launch: status slots [0, num_ctas) are its
-  int total_cost;    // decode/verify: length of the plan's cost axis (see SeqSpan)
-  int pad[62];
-};
-
-// A sequence's place on the split plan's cost axis: all sequences laid end to end, each as
-// kUnitCost units of fixed cost followed by its 128-key blocks (an empty sequence takes no
-// room). first_block is the position of its first block; CTA c owns the positions
-// [c * total_cost / n, (c + 1) * total_cost / n).
-struct SeqSpan {
-  int first_block, num_blocks;
+  int pad[63];
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -48,12 +39,11 @@ inline size_t qimg_bytes(int rp) { return align_up((size_t)2 * rp * MLA_D + size
 
 // Offsets of the workspace regions for one call.
 //   status:   one word per CTA, written by that CTA at exit (0 or its first error)
-//   seqs:     [B] SeqSpan, for the merge
 //   qimg:     one staged query image per CTA
 //   part_*:   two partial slots per CTA (the first and the last unit of its block range
 //             are the only ones that can hold part of a sequence), R rows each
 struct WsLayout {
-  size_t hdr, status, seqs, qimg, part_lse, part_out, total;
+  size_t hdr, status, qimg, part_lse, part_out, total;
   size_t qimg_stride;
   int max_slots;
 };
@@ -69,8 +59,6 @@ inline WsLayout ws_layout(int B, int rows_per_seq, int num_sms) {
   off += sizeof(unsigned) * (size_t)num_sms;
   w.qimg = off = align_up(off, 256);
   off += w.qimg_stride * (size_t)num_sms;
-  w.seqs = off = align_up(off, 256);
-  off += sizeof(SeqSpan) * (size_t)(B > 0 ? B : 1);
   w.part_lse = off = align_up(off, 256);
   off += sizeof(float) * (size_t)w.max_slots * rows_per_seq;
   w.part_out = off = align_up(off, 256);
@@ -114,7 +102,6 @@ struct AttnParams {
   float* part_out;    // [slots][part_rows][512]
   float* part_lse;    // [slots][part_rows]
   int part_rows;      // rows of a partial slot: R (decode/verify), 48 (prefill)
-  SeqSpan* seqs;      // [B]
   unsigned* status;   // [num_ctas]
   uint8_t* qimg;      // [num_ctas] staged query images, qimg_stride bytes apart
   int64_t qimg_stride;
@@ -128,17 +115,21 @@ struct AttnParams {
 };
 
 // Per-CTA stamps of the profiling hook (mla_set_trace_buffer), in nanoseconds of the GPU's
-// global timer: entry, end of the wait on the previous kernel, end of the split plan, the
-// first tile's scores read by the softmax, the last tile's probabilities written, the last
-// values MMA done, end of the last epilogue, exit; the tiles and units the CTA processed;
-// end of the first unit's epilogue and the second unit's first scores (CTAs with two units
-// or more).
+// global timer: entry, end of the wait on the previous kernel, end of the split plan (with
+// the first tile loads issued), the first tile's scores read by the softmax, the last tile's
+// probabilities written, the last values MMA done, end of the last epilogue, exit; the
+// tiles and units the CTA processed; end of the first unit's epilogue and the second unit's
+// first scores (CTAs with two units or more); decode/verify: end of the plan's scan, end of
+// its L2 prefetches.
 constexpr int kTraceWords = 16;
 enum TraceSlot { kTrEntry = 0, kTrWaited, kTrPlanned, kTrFirstScores, kTrLastP, kTrLastPV,
-                 kTrEpilogue, kTrExit, kTrCounts, kTrUnit1End, kTrUnit2Scores };
+                 kTrEpilogue, kTrExit, kTrCounts, kTrUnit1End, kTrUnit2Scores, kTrPlanScan,
+                 kTrPlanPrefetch };
 
-// The CTA of a split plan that holds block x, when `total` blocks are cut into n ranges
-// [c * total / n, (c + 1) * total / n): the largest c whose range starts at or before x.
+// The split plan's cost axis: all sequences laid end to end, each as kUnitCost units of
+// fixed cost followed by its 128-key blocks (an empty sequence takes no room); CTA c owns
+// the positions [c * total / n, (c + 1) * total / n). range_of(x): the CTA that holds
+// position x, the largest c whose range starts at or before x.
 __host__ __device__ __forceinline__ int64_t range_lo(int64_t c, int64_t total, int64_t n) {
   return c * total / n;
 }
